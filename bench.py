@@ -1,0 +1,436 @@
+"""Benchmark of the PTB forward pass (y = x + MLP(LN(x)) + Attn(LN(x)), causal
+sliding-window attention) on GB300.
+
+One step = one full layer forward (LayerNorm, [QKV | up] GEMM + GELU,
+banded SWA, [out | down] GEMM + residual) over one micro-batch of the
+175B-shaped layer of MegaScale's Table 1 (hidden 12288, 128 heads x 96,
+MLP 4H, seq 2048, window 1024) with synthetic seeded bf16 inputs resident
+in HBM.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload 175b|13b|530b|tiny|swa]
+
+--impl reference times the fp64 CPU oracle (the only other implementation
+there is) on a bounded sample of the same workload on the host's cores.
+Under torchrun each rank runs an independent replica of the layer (weak
+scaling, no collective in the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from block_sliding_window_gb300 import workloads  # noqa: E402
+
+METRIC = "PTB-layer fwd tokens/s and TFLOP/s (bf16) on 1 GB300; % of tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+GEMM_SRC = os.path.join(ROOT, "block_sliding_window_gb300", "csrc", "gemm_tcgen05.cu")
+SWA_SRC = os.path.join(ROOT, "block_sliding_window_gb300", "csrc", "swa.cu")
+
+
+def layer_flops(cfg) -> dict:
+    """Algorithmic forward FLOPs: exact GEMMs plus in-band attention only."""
+    t, h, f, w, s = cfg.tokens, cfg.hidden, cfg.ffn, cfg.window, cfg.seq
+    band = sum(min(i + 1, w) for i in range(s))
+    gemm1 = 2 * t * h * (3 * h + f)
+    gemm2 = 2 * t * (h + f) * h
+    attn = 4 * cfg.batch * h * band
+    return {"gemm1": gemm1, "gemm2": gemm2, "attn": attn, "total": gemm1 + gemm2 + attn,
+            "band_keys": band * cfg.batch * cfg.heads}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sha_of(path: str) -> str:
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str, src: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel; else None."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            entries = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    for e in entries:
+        if e.get("kernel") == kernel and e.get("workload") == workload:
+            if e.get("source_sha") == sha_of(src):
+                return e.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, busy_sm, reasons = [], [], [], set()
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                cur, top, util = float(parts[0]), float(parts[1]), float(parts[3])
+            except ValueError:
+                continue
+            sm.append(cur)
+            mx.append(top)
+            if util > 0:
+                busy_sm.append(cur)
+                for n, v in zip(names, parts[4:]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return None
+        pool = busy_sm or sm
+        return {"sm_mhz": statistics.median(pool), "sm_max_mhz": max(mx), "samples": len(sm),
+                "samples_under_load": len(busy_sm), "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_config(name: str):
+    if name == "swa":
+        return workloads.SWA_CONFIGS["swa"]
+    return workloads.PTB_CONFIGS[name]
+
+
+def config_json(name: str, cfg, world: int) -> dict:
+    if name == "swa":
+        return {"workload": (f"SWA operator alone: batch {cfg.batch}, {cfg.heads} heads x "
+                             f"{cfg.head_dim}, seq {cfg.seq}, causal window {cfg.window}"),
+                "batch": cfg.batch, "seq_len": cfg.seq, "heads": cfg.heads,
+                "head_dim": cfg.head_dim, "window": cfg.window,
+                "l2": "L2 flushed between steps (256 MB buffer written)",
+                "parallelism": f"replicas x{world}"}
+    return {"workload": (f"PTB layer forward, {cfg.name} shape: micro-batch {cfg.batch}, seq "
+                         f"{cfg.seq}, hidden {cfg.hidden}, {cfg.heads} heads x {cfg.head_dim}, "
+                         f"MLP {cfg.hidden}->{cfg.ffn}->{cfg.hidden} tanh-GELU, causal SWA window "
+                         f"{cfg.window}"),
+            "batch": cfg.batch, "seq_len": cfg.seq, "hidden": cfg.hidden, "heads": cfg.heads,
+            "ffn": cfg.ffn, "window": cfg.window, "tokens_per_step_per_gpu": cfg.tokens,
+            "l2": (f"inputs larger than L2: {2 * (4 * cfg.hidden ** 2 + 2 * cfg.hidden * cfg.ffn) / 1e9:.2f}"
+                   " GB of weights streamed every step"),
+            "parallelism": f"replicas x{world} (independent layers, no collective)"}
+
+
+# ---------------------------------------------------------------- oracle leg --
+
+def oracle_sample(cfg, rows: int, seed_device="cpu"):
+    """Host fp64 copies of the layer's inputs for the oracle (not timed)."""
+    import numpy as np
+    host = workloads.ptb_inputs(cfg, device=seed_device)
+    f64 = {k: v.detach().to("cpu").double().numpy() for k, v in host.items()}
+    f64["x"] = np.ascontiguousarray(f64["x"][:, :rows])
+    return f64
+
+
+def time_oracle(cfg, f64, rows: int, repeats: int):
+    import oracle
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle.ptb_forward(f64["x"], f64["ln_gamma"], f64["ln_beta"], f64["w_qkv"], f64["w_o"],
+                           f64["w_up"], f64["w_down"], cfg.heads, cfg.window,
+                           rows=list(range(rows)))
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def cpu_threads() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def sample_desc(cfg, rows):
+    return (f"rows 0..{rows - 1} of batch 0 of the {cfg.name} layer (LN, Q/K/V, banded softmax over"
+            f" the keys those rows see, out/up/down projections, all weights), fp64, numpy BLAS")
+
+
+def run_reference(args, world, rank):
+    """The oracle, as it stands, timed on the host cores."""
+    if rank != 0:
+        return
+    name = args.workload if args.workload != "swa" else "175b"
+    cfg = workload_config(name)
+    rows = args.cpu_rows
+    f64 = oracle_sample(cfg, rows, seed_device="cuda" if torch.cuda.is_available() else "cpu")
+    time_oracle(cfg, f64, rows, max(0, min(args.warmup, 1)))
+    times = time_oracle(cfg, f64, rows, args.steps)
+    per_step = sum(times) / len(times)
+    value = rows / per_step
+    fl = layer_flops(cfg)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "tflops": value * fl["total"] / cfg.tokens / 1e12,
+        "config": config_json(name, cfg, 1),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(),
+                         "kind": "oracle", "sample": sample_desc(cfg, rows)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------- CUDA path --
+
+def run_swa(args, world, rank, local):
+    import block_sliding_window_gb300 as bsw
+    cfg = workload_config("swa")
+    q, k, v = workloads.swa_inputs(cfg.batch, cfg.heads, cfg.seq, cfg.head_dim, cfg.seed,
+                                   device="cuda")
+    o = torch.empty_like(q)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        bsw.swa_attention(q, k, v, cfg.window, o=o)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record(stream)
+        bsw.swa_attention(q, k, v, cfg.window, o=o)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    kern_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    ms = max_over_ranks(kern_ms, world)
+    band = sum(min(i + 1, cfg.window) for i in range(cfg.seq))
+    tokens = cfg.batch * cfg.seq
+    flops = 4 * cfg.batch * cfg.heads * cfg.head_dim * band
+    bytes_ = 4 * q.numel() * 2
+    peaks, peak_src = load_peaks()
+    ach = bytes_ / (kern_ms * 1e-3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "SWA operator tokens/s (bf16) on 1 GB300", "value": tokens * world / (ms * 1e-3),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "config": config_json("swa", cfg, world),
+            "tflops": flops / (ms * 1e-3) / 1e12,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"], "peak_source": peak_src,
+                         "traffic": traffic_for("swa_kernel", "swa", SWA_SRC)},
+            "clocks": clk, "gpu_launches": args.steps}), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import block_sliding_window_gb300 as bsw
+    from block_sliding_window_gb300 import build as _build
+    _build.build()
+    bsw.load()
+    if args.workload == "swa":
+        return run_swa(args, world, rank, local)
+    cfg = workload_config(args.workload)
+    d = workloads.ptb_inputs(cfg, device="cuda")
+    ws = torch.empty(bsw.workspace_size(cfg.batch, cfg.seq, cfg.hidden, cfg.ffn),
+                     dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(d["x"])
+    fwd_args = (d["x"], d["ln_gamma"], d["ln_beta"], d["w_qkv"], d["w_o"], d["w_up"],
+                d["w_down"], cfg.heads, cfg.window)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        bsw.ptb_forward(*fwd_args, y=y, workspace=ws)
+    torch.cuda.synchronize()
+    if bsw.last_device_error() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # Timed region: K steps, per-kernel events recorded on the launching stream.
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        bsw.ptb_forward_events(*fwd_args, marks[i], y=y, workspace=ws)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    status = bsw.last_device_error()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    ms_local = t_start.elapsed_time(t_end) / args.steps
+    ms = max_over_ranks(ms_local, world)
+    names = ["layernorm", "gemm_qkv_up", "swa", "gemm_out_down"]
+    per_kernel = {n: sum(m[j].elapsed_time(m[j + 1]) for m in marks) / args.steps
+                  for j, n in enumerate(names)}
+
+    # End to end through the public call with host buffers: H2D of x, the
+    # layer, D2H of y, every step.
+    x_host = d["x"].cpu().pin_memory()
+    y_host = torch.empty(d["x"].shape, dtype=torch.bfloat16, pin_memory=True)
+    x_dev = torch.empty_like(d["x"])
+    e2e_args = (x_dev,) + fwd_args[1:]
+    for _ in range(max(1, args.warmup)):
+        x_dev.copy_(x_host, non_blocking=True)
+        bsw.ptb_forward(*e2e_args, y=y, workspace=ws)
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        bsw.ptb_forward(*e2e_args, y=y, workspace=ws)
+        y_host.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+
+    fl = layer_flops(cfg)
+    peaks, peak_src = load_peaks()
+    tokens = cfg.tokens * world
+    value = tokens / (ms * 1e-3)
+    tflops = fl["total"] * world / (ms * 1e-3) / 1e12
+    g1_ms = per_kernel["gemm_qkv_up"]
+    g1_tf = fl["gemm1"] / (g1_ms * 1e-3) / 1e12
+    peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_json(args.workload, cfg, world),
+        "tflops": tflops,
+        "pct_of_peak": {"burst": 100 * tflops / world / peaks["bf16_tflops"],
+                        "sustained": 100 * tflops / world / peak_sus, "source": peak_src},
+        "kernels_ms": per_kernel,
+        "roofline": {"bound": "tensor", "kernel": "gemm_qkv_up (tcgen05 [QKV|up] GEMM + GELU)",
+                     "achieved": g1_tf, "peak": peak_sus, "unit": "TFLOP/s",
+                     "frac": g1_tf / peak_sus, "peak_source": f"{peak_src} bf16 sustained",
+                     "traffic": traffic_for("gemm_qkv_up", args.workload, GEMM_SRC),
+                     "algorithmic_flops_per_launch": fl["gemm1"]},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2},
+        "clocks": clk,
+        "gpu_launches": 4 * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f64 = oracle_sample(cfg, args.cpu_rows, seed_device="cuda")
+        times = time_oracle(cfg, f64, args.cpu_rows, 1)
+        cpu_v = args.cpu_rows / times[0]
+        line["cpu_baseline"] = {"value": cpu_v, "unit": "tokens/s", "cores": cpu_threads(),
+                                "kind": "oracle", "sample": sample_desc(cfg, args.cpu_rows),
+                                "seconds": times[0]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["175b", "13b", "530b", "tiny", "swa"], default="175b")
+    ap.add_argument("--cpu-rows", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

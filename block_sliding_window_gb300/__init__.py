@@ -1,0 +1,259 @@
+"""GB300-native forward pass of MegaScale's parallel transformer block (PTB)
+with causal sliding-window attention (SWA).
+
+    y = x + MLP(LN(x)) + Attn(LN(x))       (MegaScale study notes, §2.2, PTB row)
+
+Thin Python binding over the C ABI of libptb.so (include/ptb.h).  It only
+marshals arguments: torch tensors provide device memory and the current
+stream, and every step of the computation runs in the library's CUDA
+kernels.  There is no fallback: if libptb.so is missing or cannot be
+loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "PTBError", "load", "ptb_forward", "ptb_forward_events", "swa_attention",
+    "swa_attention_strided", "swa_attention_counts", "layernorm", "gemm_qkv_up",
+    "gemm_out_down", "workspace_size", "release_workspace", "last_device_error",
+    "wait_probe", "LIB_PATH", "SYMBOLS",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libptb.so")
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_f32 = ctypes.c_float
+_sz = ctypes.c_size_t
+_st = ctypes.c_int
+
+# Every entry point of include/ptb.h with its ctypes signature.
+SYMBOLS = {
+    "ptb_status_string": (ctypes.c_char_p, [_st]),
+    "ptb_forward_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
+    "ptb_forward": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p]),
+    "ptb_forward_events": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p, _p, _i32]),
+    "ptb_release_workspace": (_st, []),
+    "swa_attention": (_st, [_p, _p, _p, _i64, _i32, _i64, _i32, _i32, _f32, _p, _p]),
+    "swa_attention_strided": (_st, [_p, _i64, _i64, _i64] * 4 + [_i64, _i32, _i64, _i32, _i32, _f32, _p]),
+    "swa_attention_counts": (_st, [_p, _p, _p, _i64, _i32, _i64, _i32, _i32, _f32, _p, _p, _p]),
+    "ptb_layernorm": (_st, [_p, _p, _p, _i64, _i64, _f32, _p, _p]),
+    "ptb_gemm_qkv_up": (_st, [_p, _p, _p, _i64, _i64, _i64, _p, _p]),
+    "ptb_gemm_out_down": (_st, [_p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p, _p]),
+    "ptb_last_device_error": (_st, []),
+    "ptb_wait_probe": (_st, [ctypes.c_uint64, _p]),
+}
+
+STATUS_NAMES = {0: "PTB_OK", 1: "PTB_ERR_ARG", 2: "PTB_ERR_SHAPE", 3: "PTB_ERR_ALIGN",
+                4: "PTB_ERR_WORKSPACE", 5: "PTB_ERR_LAUNCH", 6: "PTB_ERR_TIMEOUT",
+                7: "PTB_ERR_UNSUPPORTED", 8: "PTB_ERR_DEVICE"}
+
+_lib = None
+
+
+class PTBError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.ptb_status_string(status).decode() if _lib else STATUS_NAMES.get(status, "?")
+        super().__init__(f"{where}: {msg}")
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libptb.so (once) and declares every entry point's signature."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SYMBOLS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise PTBError(status, where)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _bf16_cuda(name: str, t: torch.Tensor, contiguous: bool = True) -> None:
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace_size(batch: int, seq: int, hidden: int, ffn: int) -> int:
+    return int(load().ptb_forward_workspace_size(batch, seq, hidden, ffn))
+
+
+def _ptb_args(x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, heads, window, y, workspace):
+    for n, t in (("x", x), ("ln_gamma", ln_gamma), ("ln_beta", ln_beta), ("w_qkv", w_qkv),
+                 ("w_o", w_o), ("w_up", w_up), ("w_down", w_down)):
+        _bf16_cuda(n, t)
+    if x.dim() != 3:
+        raise ValueError("x must be [batch, seq, hidden]")
+    batch, seq, hidden = x.shape
+    ffn = w_up.shape[0]
+    if (tuple(w_qkv.shape) != (3 * hidden, hidden) or tuple(w_o.shape) != (hidden, hidden)
+            or tuple(w_up.shape) != (ffn, hidden) or tuple(w_down.shape) != (hidden, ffn)
+            or ln_gamma.numel() != hidden or ln_beta.numel() != hidden):
+        raise ValueError("weight shapes do not match x")
+    if y is None:
+        y = torch.empty_like(x)
+    _bf16_cuda("y", y)
+    ws_bytes = 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    return (batch, seq, hidden, ffn), y, ws_bytes
+
+
+def ptb_forward(x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, heads: int, window: int,
+                y=None, workspace=None, stream=None) -> torch.Tensor:
+    """y = x + Attn(LN(x)) + MLP(LN(x)) on the current device; returns y."""
+    lib = load()
+    (batch, seq, hidden, ffn), y, ws_bytes = _ptb_args(
+        x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, heads, window, y, workspace)
+    st = lib.ptb_forward(_ptr(x), _ptr(ln_gamma), _ptr(ln_beta), _ptr(w_qkv), _ptr(w_o),
+                         _ptr(w_up), _ptr(w_down), batch, seq, hidden, ffn, heads, window,
+                         _ptr(y), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "ptb_forward")
+    return y
+
+
+def ptb_forward_events(x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, heads: int,
+                       window: int, events, y=None, workspace=None, stream=None):
+    """ptb_forward that also records 5 torch.cuda.Event objects at the kernel
+    boundaries (before LN, GEMM1, SWA, GEMM2 and after GEMM2)."""
+    lib = load()
+    (batch, seq, hidden, ffn), y, ws_bytes = _ptb_args(
+        x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, heads, window, y, workspace)
+    if len(events) != 5:
+        raise ValueError("need 5 events")
+    handles = (ctypes.c_void_p * 5)(*[ev.cuda_event for ev in events])
+    st = lib.ptb_forward_events(_ptr(x), _ptr(ln_gamma), _ptr(ln_beta), _ptr(w_qkv), _ptr(w_o),
+                                _ptr(w_up), _ptr(w_down), batch, seq, hidden, ffn, heads, window,
+                                _ptr(y), _ptr(workspace), ws_bytes, _stream(stream), handles, 5)
+    _check(st, "ptb_forward_events")
+    return y
+
+
+def swa_attention(q, k, v, window: int, scale: float = 0.0, o=None, stream=None):
+    """Causal sliding-window attention over [B, heads, s, d] bf16 tensors."""
+    lib = load()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _bf16_cuda(n, t)
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must be [batch, heads, seq, head_dim] of one shape")
+    if o is None:
+        o = torch.empty_like(q)
+    _bf16_cuda("o", o)
+    b, h, s, d = q.shape
+    st = lib.swa_attention(_ptr(q), _ptr(k), _ptr(v), b, h, s, d, window, scale, _ptr(o),
+                           _stream(stream))
+    _check(st, "swa_attention")
+    return o
+
+
+def swa_attention_strided(q, k, v, o, window: int, scale: float = 0.0, stream=None):
+    """SWA on strided [B, heads, s, d] views (last dim contiguous)."""
+    lib = load()
+    args = []
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _bf16_cuda(n, t, contiguous=False)
+        if t.dim() != 4 or t.stride(3) != 1:
+            raise ValueError(f"{n} must be 4-D with a contiguous last dimension")
+        args += [_ptr(t), t.stride(0), t.stride(1), t.stride(2)]
+    b, h, s, d = q.shape
+    st = lib.swa_attention_strided(*args, b, h, s, d, window, scale, _stream(stream))
+    _check(st, "swa_attention_strided")
+    return o
+
+
+def swa_attention_counts(q, k, v, window: int, scale: float = 0.0, stream=None):
+    """Runs the attention kernel with its per-row attended-key counter on;
+    returns (o, counts[B, heads, s] int32)."""
+    lib = load()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _bf16_cuda(n, t)
+    b, h, s, d = q.shape
+    o = torch.empty_like(q)
+    counts = torch.full((b, h, s), -1, dtype=torch.int32, device=q.device)
+    st = lib.swa_attention_counts(_ptr(q), _ptr(k), _ptr(v), b, h, s, d, window, scale,
+                                  _ptr(o), _ptr(counts), _stream(stream))
+    _check(st, "swa_attention_counts")
+    return o, counts
+
+
+def layernorm(x, gamma, beta, eps: float = 1e-5, out=None, stream=None):
+    lib = load()
+    _bf16_cuda("x", x)
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden
+    if out is None:
+        out = torch.empty_like(x)
+    st = lib.ptb_layernorm(_ptr(x), _ptr(gamma), _ptr(beta), rows, hidden, eps, _ptr(out),
+                           _stream(stream))
+    _check(st, "ptb_layernorm")
+    return out
+
+
+def gemm_qkv_up(xn, w_qkv, w_up, u=None, stream=None):
+    """u = [xn w_qkv^T | gelu_tanh(xn w_up^T)] for xn [T, H]."""
+    lib = load()
+    tokens, hidden = xn.shape
+    ffn = w_up.shape[0]
+    if u is None:
+        u = torch.empty(tokens, 3 * hidden + ffn, dtype=torch.bfloat16, device=xn.device)
+    st = lib.ptb_gemm_qkv_up(_ptr(xn), _ptr(w_qkv), _ptr(w_up), tokens, hidden, ffn, _ptr(u),
+                             _stream(stream))
+    _check(st, "ptb_gemm_qkv_up")
+    return u
+
+
+def gemm_out_down(ctx, g, w_o, w_down, x, y=None, stream=None):
+    """y = x + ctx w_o^T + g w_down^T (ctx, g may be row-strided views)."""
+    lib = load()
+    tokens, hidden = x.shape
+    ffn = w_down.shape[1]
+    if y is None:
+        y = torch.empty_like(x)
+    st = lib.ptb_gemm_out_down(_ptr(ctx), ctx.stride(0), _ptr(g), g.stride(0), _ptr(w_o),
+                               _ptr(w_down), _ptr(x), tokens, hidden, ffn, _ptr(y),
+                               _stream(stream))
+    _check(st, "ptb_gemm_out_down")
+    return y
+
+
+def release_workspace() -> None:
+    _check(load().ptb_release_workspace(), "ptb_release_workspace")
+
+
+def last_device_error() -> int:
+    """Synchronises and returns (and clears) the kernels' device status word."""
+    return int(load().ptb_last_device_error())
+
+
+def wait_probe(limit_ns: int, stream=None) -> None:
+    _check(load().ptb_wait_probe(limit_ns, _stream(stream)), "ptb_wait_probe")

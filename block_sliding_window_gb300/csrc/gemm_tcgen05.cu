@@ -1,0 +1,295 @@
+// The two GEMMs of the parallel transformer block on tcgen05 tensor cores.
+//
+//   [QKV | up]  : U = [xn W_qkv^T | gelu_tanh(xn W_up^T)]      (one GEMM, N = 3H + F)
+//   [out | down]: y = x + [ctx | G] [W_o | W_down]^T            (one GEMM, K = H + F)
+//
+// The PTB computes the attention and MLP branches from the same LN(x) and
+// sums both with the residual (MegaScale study notes, ch.2 §2.2, PTB row),
+// so the two input projections share one GEMM and the two output
+// projections share one GEMM whose epilogue adds x.  GeLU is fused into the
+// first GEMM's epilogue (§2.5, Table 3, efficient-operators row).
+//
+// Kernel structure (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: 128 x 64 A tile and BN x 64 B tile per stage
+//               into a ring of shared-memory stages (128-byte swizzle).
+//   warp 1      owns the TMEM allocation; one thread issues tcgen05.mma
+//               (M = 128, N = BN, K = 16) into a double-buffered fp32
+//               accumulator in TMEM and commits stage / tile completion to
+//               mbarriers.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4) .. +31, i.e. one output row per thread),
+//               GELU or residual add in fp32, bf16 stores.  The epilogue of
+//               tile i overlaps the main loop of tile i+1.
+// Every mbarrier wait is bounded (see mbar_wait); on a timeout all roles
+// unwind, wait for their own copies and MMAs, free TMEM and return.
+#include "ptb_device.cuh"
+
+namespace ptb {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // bf16 elements in one 128-byte swizzle row
+constexpr int UMMA_K = 16;
+constexpr int kThreads = 192;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes + 1024;
+};
+
+__device__ __forceinline__ float gelu_tanh(float z) {
+  const float k0 = 0.7978845608028654f;  // sqrt(2 / pi)
+  const float k1 = 0.044715f;
+  return 0.5f * z * (1.0f + tanhf(k0 * (z + k1 * z * z * z)));
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* empty_bar = full_bar + C::kStages;
+  uint64_t* tfull_bar = empty_bar + C::kStages;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* done_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_m = (p.M + BM - 1) / BM;
+  const int num_n = p.N / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 4);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.a0);
+    tma_prefetch_desc(&p.a1);
+    tma_prefetch_desc(&p.b0);
+    tma_prefetch_desc(&p.b1);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto stage_a = [&](int s) { return smem + s * C::kStageBytes; };
+  auto stage_b = [&](int s) { return smem + s * C::kStageBytes + C::kABytes; };
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      const uint64_t pol = p.epilogue == kEpiQkvGelu ? l2_policy_evict_last()
+                                                     : l2_policy_evict_first();
+      const uint64_t pol_b = l2_policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0;  // bit s: stage s has had a load issued
+      uint32_t armed_parity = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int m0 = (tile % num_m) * BM;
+        const int n0 = (tile / num_m) * BN;
+        const bool nlo = n0 < p.n_split;
+        const int by = nlo ? n0 : n0 - p.n_split;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const int k = kb * BK;
+          const bool klo = k < p.k_split;
+          const int kx = klo ? k : k - p.k_split;
+          mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
+          tma_load_2d(stage_a(stage), klo ? &p.a0 : &p.a1, &full_bar[stage], kx, m0, pol);
+          tma_load_2d(stage_b(stage), (nlo && klo) ? &p.b0 : &p.b1, &full_bar[stage], kx, by,
+                      pol_b);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Unwinding: let every copy this thread issued land before the CTA
+        // (and its shared memory) goes away.
+        volatile int no_abort = 0;
+        for (int s = 0; s < C::kStages; ++s)
+          if (armed & (1u << s))
+            mbar_wait(&full_bar[s], (armed_parity >> s) & 1u, &no_abort, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int local = 0;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sw128_kmajor_desc(smem_addr(stage_a(stage)));
+          const uint64_t bdesc = sw128_kmajor_desc(smem_addr(stage_b(stage)));
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // +32 bytes along K inside the swizzled row = +2 in the
+            // descriptor's 16-byte address units.
+            umma_bf16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          }
+          umma_commit(&empty_bar[stage]);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit(&tfull_bar[acc]);
+      }
+      // Wait for every MMA this thread issued before TMEM is released.
+      umma_commit(done_bar);
+      volatile int no_abort = 0;
+      mbar_wait(done_bar, 0, &no_abort, p.status);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue --
+    const int quarter = warp & 3;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int m0 = (tile % num_m) * BM;
+      const int n0 = (tile / num_m) * BN;
+      const int row = m0 + quarter * 32 + lane;
+      const uint32_t t_row =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c, r);
+        tmem_ld_wait();
+        if (row < p.M) {
+          const int col = n0 + c;
+          uint32_t packed[16];
+          if constexpr (EPI == kEpiQkvGelu) {
+            if (col >= p.gelu_col) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                packed[j] = pack_bf16x2(gelu_tanh(__uint_as_float(r[2 * j])),
+                                        gelu_tanh(__uint_as_float(r[2 * j + 1])));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                packed[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            }
+          } else {
+            const uint4* src = reinterpret_cast<const uint4*>(p.resid + row * p.ld_resid + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint4 x = __ldg(src + v);
+              const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int e = v * 8 + j * 2;
+                packed[v * 4 + j] = pack_bf16x2(__uint_as_float(r[e]) + bf16_lo(xs[j]),
+                                                __uint_as_float(r[e + 1]) + bf16_hi(xs[j]));
+              }
+            }
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.ld_out + col);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                packed[4 * v + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int BN, int EPI>
+cudaError_t launch_typed(const GemmArgs& a, cudaStream_t stream) {
+  using C = Cfg<BN>;
+  auto kern = gemm_kernel<BN, EPI>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  kern<<<a.grid, kThreads, C::kSmemBytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
+  if (a.epilogue == kEpiQkvGelu) {
+    switch (a.block_n) {
+      case 256: return launch_typed<256, kEpiQkvGelu>(a, stream);
+      case 128: return launch_typed<128, kEpiQkvGelu>(a, stream);
+      case 64: return launch_typed<64, kEpiQkvGelu>(a, stream);
+    }
+  } else {
+    switch (a.block_n) {
+      case 256: return launch_typed<256, kEpiResidual>(a, stream);
+      case 128: return launch_typed<128, kEpiResidual>(a, stream);
+      case 64: return launch_typed<64, kEpiResidual>(a, stream);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ptb

@@ -1,0 +1,483 @@
+// C ABI of libptb (declared in include/ptb.h): argument checks, tensor-map
+// encoding, the per-device workspace arena and status word, and the launch
+// sequence of the parallel transformer block forward pass
+//   y = x + Attn(LN(x)) + MLP(LN(x))
+// (MegaScale study notes, ch.2 §2.2, PTB row).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "ptb_device.cuh"
+
+namespace ptb {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kAlign = 256;
+
+__device__ unsigned g_status_word;
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  unsigned* status = nullptr;
+  void* arena = nullptr;
+  size_t arena_bytes = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Per-device set-up: SM count, device status word, architecture check and the
+// driver's tensor-map encoder.  Returns PTB_OK and fills *out.
+ptb_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PTB_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PTB_ERR_DEVICE;
+    if (major != 10 || minor != 3) return PTB_ERR_UNSUPPORTED;
+    void* sym = nullptr;
+    if (cudaGetSymbolAddress(&sym, g_status_word) != cudaSuccess) return PTB_ERR_DEVICE;
+    s.status = static_cast<unsigned*>(sym);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return PTB_ERR_DEVICE;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    s.ready = true;
+  }
+  *out = &s;
+  return PTB_OK;
+}
+
+// 2-D bf16 tensor map over a row-major [outer, inner] matrix with row stride
+// `ld` elements, read in boxes of 64 (inner) x box_outer with 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+              uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {64, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int pick_block_n(int64_t a, int64_t b) {
+  for (int bn : {256, 128, 64})
+    if (a % bn == 0 && b % bn == 0) return bn;
+  return 0;
+}
+
+ptb_status launch_status(cudaError_t e) { return e == cudaSuccess ? PTB_OK : PTB_ERR_LAUNCH; }
+
+const __nv_bfloat16* bf(const ptb_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
+__nv_bfloat16* bf(ptb_bf16* p) { return reinterpret_cast<__nv_bfloat16*>(p); }
+
+bool head_dim_ok(int64_t d) { return d == 16 || d == 32 || d == 64 || d == 96 || d == 128; }
+
+ptb_status gemm_qkv_up(DeviceState* ds, const ptb_bf16* xn, const ptb_bf16* w_qkv,
+                       const ptb_bf16* w_up, int64_t tokens, int64_t hidden, int64_t ffn,
+                       ptb_bf16* u, cudaStream_t stream) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.block_n = pick_block_n(3 * hidden, ffn);
+  if (!a.block_n) return PTB_ERR_SHAPE;
+  const int64_t n = 3 * hidden + ffn;
+  if (!make_map(&a.a0, xn, hidden, tokens, hidden, 128) ||
+      !make_map(&a.a1, xn, hidden, tokens, hidden, 128) ||
+      !make_map(&a.b0, w_qkv, hidden, 3 * hidden, hidden, a.block_n) ||
+      !make_map(&a.b1, w_up, hidden, ffn, hidden, a.block_n))
+    return PTB_ERR_ARG;
+  a.M = static_cast<int>(tokens);
+  a.N = static_cast<int>(n);
+  a.K = static_cast<int>(hidden);
+  a.n_split = static_cast<int>(3 * hidden);
+  a.k_split = a.K;
+  a.out = bf(u);
+  a.ld_out = n;
+  a.gelu_col = static_cast<int>(3 * hidden);
+  a.epilogue = kEpiQkvGelu;
+  const int64_t tiles = (tokens + 127) / 128 * (n / a.block_n);
+  a.grid = static_cast<int>(tiles < ds->sms ? tiles : ds->sms);
+  a.status = ds->status;
+  return launch_status(launch_gemm(a, stream));
+}
+
+ptb_status gemm_out_down(DeviceState* ds, const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16* g,
+                         int64_t ld_g, const ptb_bf16* w_o, const ptb_bf16* w_down,
+                         const ptb_bf16* x, int64_t tokens, int64_t hidden, int64_t ffn,
+                         ptb_bf16* y, cudaStream_t stream) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.block_n = pick_block_n(hidden, hidden);
+  if (!a.block_n) return PTB_ERR_SHAPE;
+  if (!make_map(&a.a0, ctx, hidden, tokens, ld_ctx, 128) ||
+      !make_map(&a.a1, g, ffn, tokens, ld_g, 128) ||
+      !make_map(&a.b0, w_o, hidden, hidden, hidden, a.block_n) ||
+      !make_map(&a.b1, w_down, ffn, hidden, ffn, a.block_n))
+    return PTB_ERR_ARG;
+  a.M = static_cast<int>(tokens);
+  a.N = static_cast<int>(hidden);
+  a.K = static_cast<int>(hidden + ffn);
+  a.n_split = a.N;
+  a.k_split = static_cast<int>(hidden);
+  a.out = bf(y);
+  a.ld_out = hidden;
+  a.resid = bf(x);
+  a.ld_resid = hidden;
+  a.gelu_col = a.N;
+  a.epilogue = kEpiResidual;
+  const int64_t tiles = (tokens + 127) / 128 * (hidden / a.block_n);
+  a.grid = static_cast<int>(tiles < ds->sms ? tiles : ds->sms);
+  a.status = ds->status;
+  return launch_status(launch_gemm(a, stream));
+}
+
+ptb_status check_gemm_shape(int64_t tokens, int64_t hidden, int64_t ffn) {
+  if (tokens < 1 || hidden < 64 || ffn < 64) return PTB_ERR_ARG;
+  if (hidden % 64 || ffn % 64) return PTB_ERR_SHAPE;
+  if (tokens > (1ll << 30) || 3 * hidden + ffn > (1ll << 30)) return PTB_ERR_SHAPE;
+  return PTB_OK;
+}
+
+ptb_status swa_impl(const SwaArgs& in, float scale, cudaStream_t stream) {
+  if (!in.q || !in.k || !in.v || !in.o) return PTB_ERR_ARG;
+  if (in.batch < 1 || in.heads < 1 || in.seq < 1 || in.window < 1) return PTB_ERR_ARG;
+  if (!head_dim_ok(in.head_dim)) return PTB_ERR_SHAPE;
+  if (in.batch * static_cast<int64_t>(in.heads) > 65535) return PTB_ERR_SHAPE;
+  const int64_t strides[12] = {in.q_sb, in.q_sh, in.q_ss, in.k_sb, in.k_sh, in.k_ss,
+                               in.v_sb, in.v_sh, in.v_ss, in.o_sb, in.o_sh, in.o_ss};
+  for (int64_t s : strides)
+    if (s % 8) return PTB_ERR_ALIGN;
+  if (!aligned(in.q, 16) || !aligned(in.k, 16) || !aligned(in.v, 16) || !aligned(in.o, 16))
+    return PTB_ERR_ALIGN;
+  if (scale < 0.f || !std::isfinite(scale)) return PTB_ERR_ARG;
+  DeviceState* ds = nullptr;
+  ptb_status st = device_state(&ds);
+  if (st != PTB_OK) return st;
+  SwaArgs a = in;
+  const float sc = scale == 0.f ? 1.0f / std::sqrt(static_cast<float>(in.head_dim)) : scale;
+  a.scale_log2 = sc * 1.4426950408889634f;
+  return launch_status(launch_swa(a, stream));
+}
+
+// ----------------------------------------------------------- wait probe --
+
+__global__ void wait_probe_kernel(uint64_t limit_ns, unsigned* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Nobody arrives on `bar`: the wait must give up and record a timeout.
+    mbar_wait(&bar, 0, &abort_flag, status, limit_ns);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_wait_probe(uint64_t limit_ns, unsigned* status, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
+  return cudaGetLastError();
+}
+
+}  // namespace ptb
+
+using namespace ptb;
+
+extern "C" {
+
+const char* ptb_status_string(ptb_status s) {
+  switch (s) {
+    case PTB_OK: return "PTB_OK";
+    case PTB_ERR_ARG: return "PTB_ERR_ARG: invalid argument";
+    case PTB_ERR_SHAPE: return "PTB_ERR_SHAPE: unsupported shape";
+    case PTB_ERR_ALIGN: return "PTB_ERR_ALIGN: pointer or stride not 16-byte aligned";
+    case PTB_ERR_WORKSPACE: return "PTB_ERR_WORKSPACE: workspace too small";
+    case PTB_ERR_LAUNCH: return "PTB_ERR_LAUNCH: CUDA launch or runtime error";
+    case PTB_ERR_TIMEOUT: return "PTB_ERR_TIMEOUT: a device-side wait gave up";
+    case PTB_ERR_UNSUPPORTED: return "PTB_ERR_UNSUPPORTED: device is not sm_103";
+    case PTB_ERR_DEVICE: return "PTB_ERR_DEVICE: device query or allocation failed";
+  }
+  return "PTB_ERR_UNKNOWN";
+}
+
+size_t ptb_forward_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn) {
+  if (batch < 1 || seq < 1 || hidden < 1 || ffn < 1) return 0;
+  const size_t t = static_cast<size_t>(batch) * static_cast<size_t>(seq);
+  return round_up(t * hidden * 2, kAlign) + round_up(t * (3 * hidden + ffn) * 2, kAlign);
+}
+
+ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
+                              const ptb_bf16* ln_beta, const ptb_bf16* w_qkv,
+                              const ptb_bf16* w_o, const ptb_bf16* w_up, const ptb_bf16* w_down,
+                              int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,
+                              int32_t heads, int32_t window, ptb_bf16* y, void* workspace,
+                              size_t workspace_bytes, ptb_stream stream_, void* const* events,
+                              int32_t n_events) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (!x || !ln_gamma || !ln_beta || !w_qkv || !w_o || !w_up || !w_down || !y) return PTB_ERR_ARG;
+  if (batch < 1 || seq < 1 || heads < 1 || window < 1) return PTB_ERR_ARG;
+  ptb_status st = check_gemm_shape(batch * seq, hidden, ffn);
+  if (st != PTB_OK) return st;
+  if (hidden > 32768 || hidden % heads) return PTB_ERR_SHAPE;
+  const int64_t d = hidden / heads;
+  if (!head_dim_ok(d)) return PTB_ERR_SHAPE;
+  if (batch * static_cast<int64_t>(heads) > 65535) return PTB_ERR_SHAPE;
+  const void* ptrs[] = {x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, y};
+  for (const void* p : ptrs)
+    if (!aligned(p, 16)) return PTB_ERR_ALIGN;
+  if (events && n_events != 5) return PTB_ERR_ARG;
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != PTB_OK) return st;
+
+  const int64_t tokens = batch * seq;
+  const size_t need = ptb_forward_workspace_size(batch, seq, hidden, ffn);
+  if (workspace) {
+    if (workspace_bytes < need) return PTB_ERR_WORKSPACE;
+    if (!aligned(workspace, kAlign)) return PTB_ERR_ALIGN;
+  } else {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (ds->arena_bytes < need) {
+      if (ds->arena) {
+        cudaDeviceSynchronize();
+        cudaFree(ds->arena);
+        ds->arena = nullptr;
+        ds->arena_bytes = 0;
+      }
+      if (cudaMalloc(&ds->arena, need) != cudaSuccess) {
+        ds->arena = nullptr;
+        return PTB_ERR_DEVICE;
+      }
+      ds->arena_bytes = need;
+    }
+    workspace = ds->arena;
+  }
+  ptb_bf16* xn = static_cast<ptb_bf16*>(workspace);
+  ptb_bf16* u = reinterpret_cast<ptb_bf16*>(static_cast<char*>(workspace) +
+                                            round_up(tokens * hidden * 2, kAlign));
+  const int64_t ldu = 3 * hidden + ffn;
+  auto mark = [&](int i) {
+    if (events) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream);
+  };
+
+  // 1. xn = LN(x)
+  mark(0);
+  if (launch_layernorm(bf(x), bf(ln_gamma), bf(ln_beta), tokens, static_cast<int>(hidden), 1e-5f,
+                       bf(xn), stream) != cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  // 2. U = [xn W_qkv^T | gelu(xn W_up^T)]
+  mark(1);
+  st = gemm_qkv_up(ds, xn, w_qkv, w_up, tokens, hidden, ffn, u, stream);
+  if (st != PTB_OK) return st;
+  // 3. ctx = SWA(Q, K, V), written over Q inside U
+  mark(2);
+  SwaArgs sa;
+  std::memset(&sa, 0, sizeof(sa));
+  sa.q = bf(u);
+  sa.k = bf(u) + hidden;
+  sa.v = bf(u) + 2 * hidden;
+  sa.o = bf(u);
+  sa.q_sb = sa.k_sb = sa.v_sb = sa.o_sb = seq * ldu;
+  sa.q_sh = sa.k_sh = sa.v_sh = sa.o_sh = d;
+  sa.q_ss = sa.k_ss = sa.v_ss = sa.o_ss = ldu;
+  sa.batch = static_cast<int>(batch);
+  sa.heads = heads;
+  sa.seq = static_cast<int>(seq);
+  sa.head_dim = static_cast<int>(d);
+  sa.window = window;
+  sa.scale_log2 = (1.0f / std::sqrt(static_cast<float>(d))) * 1.4426950408889634f;
+  if (launch_swa(sa, stream) != cudaSuccess) return PTB_ERR_LAUNCH;
+  // 4. y = x + [ctx | G] [W_o | W_down]^T
+  mark(3);
+  st = gemm_out_down(ds, u, ldu, u + 3 * hidden, ldu, w_o, w_down, x, tokens, hidden, ffn, y,
+                     stream);
+  if (st != PTB_OK) return st;
+  mark(4);
+  return PTB_OK;
+}
+
+ptb_status ptb_forward(const ptb_bf16* x, const ptb_bf16* ln_gamma, const ptb_bf16* ln_beta,
+                       const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
+                       const ptb_bf16* w_down, int64_t batch, int64_t seq, int64_t hidden,
+                       int64_t ffn, int32_t heads, int32_t window, ptb_bf16* y,
+                       void* workspace, size_t workspace_bytes, ptb_stream stream) {
+  return ptb_forward_events(x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, batch, seq, hidden,
+                            ffn, heads, window, y, workspace, workspace_bytes, stream, nullptr, 0);
+}
+
+ptb_status ptb_release_workspace(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PTB_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& s = g_dev[dev];
+  if (s.arena) {
+    cudaDeviceSynchronize();
+    cudaFree(s.arena);
+    s.arena = nullptr;
+    s.arena_bytes = 0;
+  }
+  return PTB_OK;
+}
+
+ptb_status swa_attention_strided(const ptb_bf16* q, int64_t q_sb, int64_t q_sh, int64_t q_ss,
+                                 const ptb_bf16* k, int64_t k_sb, int64_t k_sh, int64_t k_ss,
+                                 const ptb_bf16* v, int64_t v_sb, int64_t v_sh, int64_t v_ss,
+                                 ptb_bf16* o, int64_t o_sb, int64_t o_sh, int64_t o_ss,
+                                 int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
+                                 int32_t window, float scale, ptb_stream stream) {
+  if (batch > 65535 || seq > (1ll << 30)) return PTB_ERR_SHAPE;
+  SwaArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = bf(q);
+  a.k = bf(k);
+  a.v = bf(v);
+  a.o = bf(o);
+  a.q_sb = q_sb; a.q_sh = q_sh; a.q_ss = q_ss;
+  a.k_sb = k_sb; a.k_sh = k_sh; a.k_ss = k_ss;
+  a.v_sb = v_sb; a.v_sh = v_sh; a.v_ss = v_ss;
+  a.o_sb = o_sb; a.o_sh = o_sh; a.o_ss = o_ss;
+  a.batch = static_cast<int>(batch);
+  a.heads = heads;
+  a.seq = static_cast<int>(seq);
+  a.head_dim = head_dim;
+  a.window = window;
+  return swa_impl(a, scale, static_cast<cudaStream_t>(stream));
+}
+
+static ptb_status swa_contiguous(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v,
+                                 int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
+                                 int32_t window, float scale, ptb_bf16* o, int32_t* counts,
+                                 ptb_stream stream) {
+  if (batch > 65535 || seq > (1ll << 30) || head_dim < 1) return batch < 1 ? PTB_ERR_ARG
+                                                                           : PTB_ERR_SHAPE;
+  if (o == q || o == k || o == v) return PTB_ERR_ARG;
+  SwaArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = bf(q);
+  a.k = bf(k);
+  a.v = bf(v);
+  a.o = bf(o);
+  const int64_t ss = head_dim, sh = seq * head_dim, sb = heads * seq * head_dim;
+  a.q_sb = a.k_sb = a.v_sb = a.o_sb = sb;
+  a.q_sh = a.k_sh = a.v_sh = a.o_sh = sh;
+  a.q_ss = a.k_ss = a.v_ss = a.o_ss = ss;
+  a.batch = static_cast<int>(batch);
+  a.heads = heads;
+  a.seq = static_cast<int>(seq);
+  a.head_dim = head_dim;
+  a.window = window;
+  a.counts = counts;
+  return swa_impl(a, scale, static_cast<cudaStream_t>(stream));
+}
+
+ptb_status swa_attention(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v, int64_t batch,
+                         int32_t heads, int64_t seq, int32_t head_dim, int32_t window,
+                         float scale, ptb_bf16* o, ptb_stream stream) {
+  return swa_contiguous(q, k, v, batch, heads, seq, head_dim, window, scale, o, nullptr, stream);
+}
+
+ptb_status swa_attention_counts(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v,
+                                int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
+                                int32_t window, float scale, ptb_bf16* o, int32_t* counts,
+                                ptb_stream stream) {
+  if (!counts || !aligned(counts, 4)) return PTB_ERR_ARG;
+  return swa_contiguous(q, k, v, batch, heads, seq, head_dim, window, scale, o, counts, stream);
+}
+
+ptb_status ptb_layernorm(const ptb_bf16* x, const ptb_bf16* gamma, const ptb_bf16* beta,
+                         int64_t rows, int64_t hidden, float eps, ptb_bf16* out,
+                         ptb_stream stream) {
+  if (!x || !gamma || !beta || !out || rows < 1 || hidden < 8 || !(eps >= 0.f))
+    return PTB_ERR_ARG;
+  if (hidden % 8 || hidden > 32768 || rows > 0x7fffffff) return PTB_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(beta, 16) || !aligned(out, 16))
+    return PTB_ERR_ALIGN;
+  DeviceState* ds = nullptr;
+  ptb_status st = device_state(&ds);
+  if (st != PTB_OK) return st;
+  return launch_status(launch_layernorm(bf(x), bf(gamma), bf(beta), rows, static_cast<int>(hidden),
+                                        eps, bf(out), static_cast<cudaStream_t>(stream)));
+}
+
+ptb_status ptb_gemm_qkv_up(const ptb_bf16* xn, const ptb_bf16* w_qkv, const ptb_bf16* w_up,
+                           int64_t tokens, int64_t hidden, int64_t ffn, ptb_bf16* u,
+                           ptb_stream stream) {
+  if (!xn || !w_qkv || !w_up || !u) return PTB_ERR_ARG;
+  ptb_status st = check_gemm_shape(tokens, hidden, ffn);
+  if (st != PTB_OK) return st;
+  if (!aligned(xn, 16) || !aligned(w_qkv, 16) || !aligned(w_up, 16) || !aligned(u, 16))
+    return PTB_ERR_ALIGN;
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != PTB_OK) return st;
+  return gemm_qkv_up(ds, xn, w_qkv, w_up, tokens, hidden, ffn, u,
+                     static_cast<cudaStream_t>(stream));
+}
+
+ptb_status ptb_gemm_out_down(const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16* g, int64_t ld_g,
+                             const ptb_bf16* w_o, const ptb_bf16* w_down, const ptb_bf16* x,
+                             int64_t tokens, int64_t hidden, int64_t ffn, ptb_bf16* y,
+                             ptb_stream stream) {
+  if (!ctx || !g || !w_o || !w_down || !x || !y) return PTB_ERR_ARG;
+  ptb_status st = check_gemm_shape(tokens, hidden, ffn);
+  if (st != PTB_OK) return st;
+  if (ld_ctx < hidden || ld_g < ffn) return PTB_ERR_ARG;
+  if (ld_ctx % 8 || ld_g % 8) return PTB_ERR_ALIGN;
+  const void* ptrs[] = {ctx, g, w_o, w_down, x, y};
+  for (const void* p : ptrs)
+    if (!aligned(p, 16)) return PTB_ERR_ALIGN;
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != PTB_OK) return st;
+  return gemm_out_down(ds, ctx, ld_ctx, g, ld_g, w_o, w_down, x, tokens, hidden, ffn, y,
+                       static_cast<cudaStream_t>(stream));
+}
+
+ptb_status ptb_last_device_error(void) {
+  DeviceState* ds = nullptr;
+  ptb_status st = device_state(&ds);
+  if (st != PTB_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PTB_ERR_LAUNCH;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  const unsigned zero = 0;
+  if (cudaMemcpy(ds->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  return static_cast<ptb_status>(word);
+}
+
+ptb_status ptb_wait_probe(uint64_t limit_ns, ptb_stream stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return PTB_ERR_ARG;
+  DeviceState* ds = nullptr;
+  ptb_status st = device_state(&ds);
+  if (st != PTB_OK) return st;
+  return launch_status(launch_wait_probe(limit_ns, ds->status, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// Internal declarations shared by the translation units of libptb.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cuda_bf16.h>
+
+#include "ptb.h"
+
+namespace ptb {
+
+// Epilogue of the tcgen05 GEMM.
+enum GemmEpilogue : int {
+  kEpiQkvGelu = 0,   // store bf16(acc); columns >= gelu_col store bf16(gelu_tanh(acc))
+  kEpiResidual = 1,  // store bf16(acc + resid)
+};
+
+// One GEMM launch: C[M, N] = A[M, K] * B[N, K]^T with A and B split into two
+// tensor maps each.  Columns n < n_split read B rows from map b0 (row n),
+// the rest from b1 (row n - n_split); inner indices k < k_split read A and B
+// from a0/b0 (column k), the rest from a1/b1 (column k - k_split).  At most
+// one of the two splits is active.
+struct GemmArgs {
+  CUtensorMap a0, a1, b0, b1;
+  int M, N, K;
+  int n_split, k_split;
+  int block_n;  // 64, 128 or 256
+  __nv_bfloat16* out;
+  int64_t ld_out;
+  const __nv_bfloat16* resid;
+  int64_t ld_resid;
+  int gelu_col;
+  int epilogue;
+  int grid;  // persistent CTAs (<= number of SMs)
+  unsigned* status;
+};
+
+struct SwaArgs {
+  const __nv_bfloat16 *q, *k, *v;
+  __nv_bfloat16* o;
+  int64_t q_sb, q_sh, q_ss, k_sb, k_sh, k_ss, v_sb, v_sh, v_ss, o_sb, o_sh, o_ss;
+  int batch, heads, seq, head_dim, window;
+  float scale_log2;  // softmax scale * log2(e)
+  int* counts;       // optional per-row attended-key counts
+};
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
+cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* gamma,
+                             const __nv_bfloat16* beta, int64_t rows, int hidden, float eps,
+                             __nv_bfloat16* out, cudaStream_t stream);
+cudaError_t launch_swa(const SwaArgs& a, cudaStream_t stream);
+cudaError_t launch_wait_probe(uint64_t limit_ns, unsigned* status, cudaStream_t stream);
+
+}  // namespace ptb

@@ -109,6 +109,23 @@ def swa_inputs(batch: int, heads: int, seq: int, head_dim: int, seed: int,
     return tuple(_normal(g, shape, std, device) for _ in range(3))
 
 
+def normal_bf16(shape, seed: int, std: float = 1.0, mean: float = 0.0,
+                device="cpu") -> torch.Tensor:
+    """One seeded N(mean, std^2) tensor rounded to bf16."""
+    t = torch.randn(*shape, generator=_generator(seed, device), dtype=torch.float32,
+                    device=device)
+    return (t * std + mean).to(torch.bfloat16)
+
+
+def sample_rows(seq: int, window: int) -> list:
+    """Sequence positions checked one by one on the full-size layers: the
+    first rows, the tile edges around 64 and 128, the window edge and the
+    last rows."""
+    cand = {0, 1, 2, 63, 64, 127, 128, 129, window - 1, window, window + 1,
+            seq // 2, seq - 2, seq - 1}
+    return sorted(r for r in cand if 0 <= r < seq)
+
+
 def small_ptb(batch: int, seq: int, hidden: int, heads: int, ffn: int,
               window: int, seed: int, w_std: float = 0.05) -> PTBConfig:
     """An ad-hoc layer shape for the tile-edge parity cases."""

@@ -1,0 +1,209 @@
+/*
+ * ptb.h - C ABI of libptb: the forward pass of MegaScale's parallel
+ * transformer block (PTB) with causal sliding-window attention (SWA), as
+ * hand-written CUDA kernels for GB300 (sm_103a).
+ *
+ * Definitions (MegaScale study notes, ai-yanyi-papers.pages.dev/papers/
+ * 18-megascale.html, ch.2 §2.2 = paper §3.1, algorithm-change table):
+ *   PTB row:  y = x + MLP(LN(x)) + Attention(LN(x))   -- one shared LN,
+ *             attention and MLP branches computed side by side and summed.
+ *   SWA row:  each token attends only to a fixed window of w positions,
+ *             cost O(s*w) rather than O(s*s).
+ * Readings fixed here: the window is causal and includes the token itself,
+ * so query row i attends to keys max(0, i-w+1) .. i (exactly min(i+1, w)
+ * keys); w >= s is plain causal attention.  Softmax scale 1/sqrt(d) unless
+ * given; MLP(u) = gelu_tanh(u W_up^T) W_down^T; LayerNorm uses the biased
+ * variance with eps = 1e-5; no biases, dropout or positional terms.
+ *
+ * Numerics: bf16 storage, fp32 accumulation in every contraction, fp32
+ * LayerNorm statistics and softmax, one round-to-nearest-even bf16 rounding
+ * per stored tensor.
+ *
+ * Common conventions
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; the
+ *     library never frees or retains caller memory.  bf16 values are passed
+ *     as raw 16-bit patterns (ptb_bf16).
+ *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL
+ *     is the legacy default stream) on the current CUDA device.  No entry
+ *     point synchronises except ptb_last_device_error().
+ *   - Argument errors are detected on the host before anything is launched
+ *     and returned as a ptb_status; nothing is written in that case.
+ *   - Kernels never trap.  A device-side wait that does not complete within
+ *     about two seconds makes the kernel give up, record PTB_ERR_TIMEOUT in
+ *     the per-device status word and return; ptb_last_device_error() reads
+ *     and clears that word.
+ */
+#ifndef PTB_H_
+#define PTB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t ptb_bf16; /* raw bfloat16 bits */
+typedef void* ptb_stream;  /* cudaStream_t */
+
+typedef enum {
+  PTB_OK = 0,
+  PTB_ERR_ARG = 1,         /* null pointer, non-positive size, bad window   */
+  PTB_ERR_SHAPE = 2,       /* shape outside the supported set (see below)   */
+  PTB_ERR_ALIGN = 3,       /* pointer or stride not 16-byte aligned         */
+  PTB_ERR_WORKSPACE = 4,   /* caller workspace smaller than required        */
+  PTB_ERR_LAUNCH = 5,      /* CUDA launch or runtime error                  */
+  PTB_ERR_TIMEOUT = 6,     /* a device-side wait gave up (kernel unwound)   */
+  PTB_ERR_UNSUPPORTED = 7, /* device is not sm_103 / sm_100 class           */
+  PTB_ERR_DEVICE = 8       /* device query or allocation failed             */
+} ptb_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* ptb_status_string(ptb_status status);
+
+/*
+ * Bytes of scratch that ptb_forward needs for this shape: the normalised
+ * activations xn [T, H] and the fused projection output U [T, 3H + F]
+ * (T = batch * seq), each bf16 and 256-byte aligned.
+ */
+size_t ptb_forward_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn);
+
+/*
+ * ptb_forward: y = x + Attn(LN(x)) + MLP(LN(x))  (PTB row, §2.2).
+ *
+ *   x        [batch, seq, hidden]   bf16, row-major (token-major)
+ *   ln_gamma [hidden], ln_beta [hidden]  LayerNorm affine parameters
+ *   w_qkv    [3*hidden, hidden]  nn.Linear layout [out, in]: rows hold all
+ *            query heads, then all key heads, then all value heads; head h
+ *            occupies rows h*d .. h*d+d-1 of each third (d = hidden/heads)
+ *   w_o      [hidden, hidden]    input columns ordered by head
+ *   w_up     [ffn, hidden], w_down [hidden, ffn]
+ *   heads    number of attention heads; d = hidden / heads must be one of
+ *            16, 32, 64, 96, 128
+ *   window   SWA window w >= 1 (w >= seq means full causal attention)
+ *   y        [batch, seq, hidden] bf16 output; must not alias any input
+ *   workspace, workspace_bytes
+ *            caller scratch of at least ptb_forward_workspace_size() bytes,
+ *            256-byte aligned; or NULL/0, in which case the library uses
+ *            an arena of its own per device, grown on demand with
+ *            cudaMalloc and kept until ptb_release_workspace().
+ *   stream   CUDA stream for every launch.
+ *
+ * Shapes: hidden and ffn multiples of 64, hidden <= 32768, batch*seq >= 1.
+ * Pointers 16-byte aligned.  Four kernels run in order on `stream`:
+ * LayerNorm, the [QKV | up] GEMM with the GELU epilogue, banded SWA, and the
+ * K-concatenated [out | down] GEMM whose epilogue adds x.
+ */
+ptb_status ptb_forward(const ptb_bf16* x, const ptb_bf16* ln_gamma, const ptb_bf16* ln_beta,
+                       const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
+                       const ptb_bf16* w_down, int64_t batch, int64_t seq, int64_t hidden,
+                       int64_t ffn, int32_t heads, int32_t window, ptb_bf16* y,
+                       void* workspace, size_t workspace_bytes, ptb_stream stream);
+
+/*
+ * Same as ptb_forward, and records `events[0..4]` (cudaEvent_t handles owned
+ * by the caller; n_events must be 5) on `stream` before the LayerNorm, the
+ * first GEMM, the attention, the second GEMM and after it, so a caller can
+ * time each kernel.
+ */
+ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
+                              const ptb_bf16* ln_beta, const ptb_bf16* w_qkv,
+                              const ptb_bf16* w_o, const ptb_bf16* w_up, const ptb_bf16* w_down,
+                              int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,
+                              int32_t heads, int32_t window, ptb_bf16* y, void* workspace,
+                              size_t workspace_bytes, ptb_stream stream, void* const* events,
+                              int32_t n_events);
+
+/* Frees the library's own workspace arena on the current device (if any). */
+ptb_status ptb_release_workspace(void);
+
+/*
+ * swa_attention: o = softmax_band(q k^T * scale) v  (SWA row, §2.2).
+ *
+ *   q, k, v, o  [batch, heads, seq, head_dim] bf16, contiguous
+ *   head_dim    one of 16, 32, 64, 96, 128
+ *   window      w >= 1; row i attends to keys max(0, i-w+1) .. i
+ *   scale       softmax scale; 0 selects 1/sqrt(head_dim)
+ * o must not alias q, k or v.
+ */
+ptb_status swa_attention(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v, int64_t batch,
+                         int32_t heads, int64_t seq, int32_t head_dim, int32_t window,
+                         float scale, ptb_bf16* o, ptb_stream stream);
+
+/*
+ * swa_attention_strided: the same operation on strided views.  Element
+ * (b, h, i, c) of tensor t lives at t[b*sb + h*sh + i*ss + c]; strides are
+ * in elements and must be multiples of 8 (16 bytes).  The PTB path uses it
+ * on the column blocks of the fused projection output.  o may alias q
+ * exactly (same pointer and strides): each query tile is read in full
+ * before its output is written and no other tile reads it.
+ */
+ptb_status swa_attention_strided(const ptb_bf16* q, int64_t q_sb, int64_t q_sh, int64_t q_ss,
+                                 const ptb_bf16* k, int64_t k_sb, int64_t k_sh, int64_t k_ss,
+                                 const ptb_bf16* v, int64_t v_sb, int64_t v_sh, int64_t v_ss,
+                                 ptb_bf16* o, int64_t o_sb, int64_t o_sh, int64_t o_ss,
+                                 int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
+                                 int32_t window, float scale, ptb_stream stream);
+
+/*
+ * swa_attention_counts: runs the attention kernel's own masking code and
+ * writes, for every row (b, h, i), how many keys passed the band mask into
+ * counts[(b*heads + h)*seq + i] (int32, device memory).  The expected value
+ * is exactly min(i+1, window).  o receives the attention output as usual.
+ */
+ptb_status swa_attention_counts(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v,
+                                int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
+                                int32_t window, float scale, ptb_bf16* o, int32_t* counts,
+                                ptb_stream stream);
+
+/*
+ * ptb_layernorm: out[r, :] = (x[r, :] - mean) / sqrt(var + eps) * gamma + beta
+ * for rows r < rows; x and out [rows, hidden] bf16 row-major; fp32
+ * statistics, biased variance.  hidden a multiple of 8 and <= 32768.
+ */
+ptb_status ptb_layernorm(const ptb_bf16* x, const ptb_bf16* gamma, const ptb_bf16* beta,
+                         int64_t rows, int64_t hidden, float eps, ptb_bf16* out,
+                         ptb_stream stream);
+
+/*
+ * ptb_gemm_qkv_up: the fused first projection of the PTB,
+ *   u[:, 0:3H]      = xn w_qkv^T
+ *   u[:, 3H:3H+F]   = gelu_tanh(xn w_up^T)
+ * xn [T, H], u [T, 3H+F] row-major bf16; H, F multiples of 64.
+ */
+ptb_status ptb_gemm_qkv_up(const ptb_bf16* xn, const ptb_bf16* w_qkv, const ptb_bf16* w_up,
+                           int64_t tokens, int64_t hidden, int64_t ffn, ptb_bf16* u,
+                           ptb_stream stream);
+
+/*
+ * ptb_gemm_out_down: the fused output projection with the residual,
+ *   y = x + ctx w_o^T + g w_down^T,
+ * one GEMM over the concatenated inner dimension [ctx | g] (H + F).
+ * ctx [T, H] with row stride ld_ctx, g [T, F] with row stride ld_g (strides
+ * in elements, multiples of 8), x and y [T, H] contiguous.
+ */
+ptb_status ptb_gemm_out_down(const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16* g, int64_t ld_g,
+                             const ptb_bf16* w_o, const ptb_bf16* w_down, const ptb_bf16* x,
+                             int64_t tokens, int64_t hidden, int64_t ffn, ptb_bf16* y,
+                             ptb_stream stream);
+
+/*
+ * Synchronises the current device, then returns and clears the device
+ * status word written by the kernels (PTB_OK if no kernel gave up), or
+ * PTB_ERR_LAUNCH if the CUDA context reports an error.
+ */
+ptb_status ptb_last_device_error(void);
+
+/*
+ * Test hook: the wait limit of the kernels' bounded waits.  ptb_wait_probe
+ * launches one CTA that waits on an mbarrier nobody signals, with a limit
+ * of `limit_ns`; it must come back with PTB_ERR_TIMEOUT recorded rather
+ * than hang.  Returns the launch status.
+ */
+ptb_status ptb_wait_probe(uint64_t limit_ns, ptb_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PTB_H_ */

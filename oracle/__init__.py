@@ -5,6 +5,6 @@ and the CPU-baseline leg of ``bench.py``; never by the product package.
 """
 from .ptb_oracle import (  # noqa: F401
     LN_EPS, attended_counts, attention_branch, band_mask, gelu_tanh,
-    layer_flops, layer_norm, mfu, mlp_branch, needed_key_positions,
+    layer_flops, layer_norm, linear, mfu, mlp_branch, needed_key_positions,
     ptb_forward, serial_block, swa, swa_weights,
 )

@@ -38,6 +38,10 @@ GELU_CUBIC = 0.044715
 
 
 def _f64(a) -> np.ndarray:
+    """float64 numpy copy of an array; torch tensors of any dtype (bf16
+    included, which numpy lacks) are converted on the host first."""
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu").double().numpy()
     return np.asarray(a, dtype=np.float64)
 
 
@@ -126,14 +130,13 @@ def swa(q, k, v, window: int, scale: float | None = None,
     return p @ _f64(v)
 
 
-def _linear(a, w) -> np.ndarray:
+def linear(a, w) -> np.ndarray:
     """a @ w.T for an nn.Linear weight w of shape [out, in] (no bias).
 
     w is upcast to float64 a slab of output rows at a time so that the
     530B-shaped weights need not exist twice in fp64; every output element
     is still one full-length dot product."""
     a = _f64(a)
-    w = np.asarray(w)
     out = np.empty(a.shape[:-1] + (w.shape[0],), dtype=np.float64)
     step = 8192
     for r0 in range(0, w.shape[0], step):
@@ -161,10 +164,9 @@ def attention_branch(u_q, u_k, w_qkv, w_o, heads: int, window: int,
     (MegaScale notes, §2.2, SWA row)."""
     bsz, _, hidden = u_q.shape
     d = hidden // heads
-    w_qkv = np.asarray(w_qkv)
-    q = _linear(u_q, w_qkv[0:hidden])
-    k = _linear(u_k, w_qkv[hidden:2 * hidden])
-    v = _linear(u_k, w_qkv[2 * hidden:3 * hidden])
+    q = linear(u_q, w_qkv[0:hidden])
+    k = linear(u_k, w_qkv[hidden:2 * hidden])
+    v = linear(u_k, w_qkv[2 * hidden:3 * hidden])
 
     def split_heads(t):  # [B, n, H] -> [B, heads, n, d]
         return t.reshape(bsz, t.shape[1], heads, d).transpose(0, 2, 1, 3)
@@ -172,12 +174,12 @@ def attention_branch(u_q, u_k, w_qkv, w_o, heads: int, window: int,
     ctx = swa(split_heads(q), split_heads(k), split_heads(v), window,
               1.0 / math.sqrt(d), q_pos, k_pos)                 # [B, heads, R, d]
     ctx = ctx.transpose(0, 2, 1, 3).reshape(bsz, len(q_pos), hidden)
-    return _linear(ctx, w_o)
+    return linear(ctx, w_o)
 
 
 def mlp_branch(u, w_up, w_down) -> np.ndarray:
     """MLP(u) = gelu_tanh(u W_up^T) W_down^T, no biases."""
-    return _linear(gelu_tanh(_linear(u, w_up)), w_down)
+    return linear(gelu_tanh(linear(u, w_up)), w_down)
 
 
 def ptb_forward(x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down,

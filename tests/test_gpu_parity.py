@@ -1,0 +1,234 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Every case feeds identical seeded bf16 inputs to both sides and compares
+element by element with relative L2 <= 1e-2 and max-abs <= 3e-2; the
+attention mask is compared bit-exactly through the kernel's own per-row
+attended-key counts and through the zero pattern of a one-hot value probe.
+Full-size layers (13B-class, 175B and 530B shapes) run in the same launch
+configuration the benchmark times and are checked on sampled rows that the
+oracle computes one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sliding_window_gb300 import workloads
+from tests.parity import assert_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _cuda(d):
+    return {k: v.cuda() for k, v in d.items()}
+
+
+@pytest.fixture(autouse=True)
+def _status_clean(ptb_lib):
+    ptb_lib.last_device_error()
+    yield
+    assert ptb_lib.last_device_error() == 0, "a kernel recorded a device-side error"
+
+
+# ------------------------------------------------------------- bounded wait --
+
+def test_bounded_wait_gives_up_and_reports(ptb_lib):
+    """A wait on an mbarrier nobody signals ends with PTB_ERR_TIMEOUT instead
+    of hanging, and the context stays usable."""
+    ptb_lib.wait_probe(20_000_000)  # 20 ms
+    assert ptb_lib.last_device_error() == 6
+    assert ptb_lib.last_device_error() == 0
+    assert torch.ones(8, device="cuda").sum().item() == 8
+
+
+# --------------------------------------------------------------- LayerNorm --
+
+@pytest.mark.parametrize("rows,hidden", [(1, 64), (3, 8), (130, 5120), (17, 12288),
+                                         (5, 20480), (2, 32768), (64, 96)])
+def test_layernorm(ptb_lib, rows, hidden):
+    x = workloads.normal_bf16((rows, hidden), seed=rows + hidden, std=2.0, mean=0.5)
+    gamma = workloads.normal_bf16((hidden,), seed=1, std=0.1, mean=1.0)
+    beta = workloads.normal_bf16((hidden,), seed=2, std=0.1)
+    out = ptb_lib.layernorm(x.cuda(), gamma.cuda(), beta.cuda())
+    assert_close(out, oracle.layer_norm(x, gamma, beta), f"LN {rows}x{hidden}")
+
+
+# ----------------------------------------------------------- [QKV | up] GEMM --
+
+GEMM_SHAPES = [(128, 64, 256), (600, 256, 1024), (257, 384, 1536), (1, 64, 64),
+               (2048, 1024, 4096), (333, 192, 320)]
+
+
+@pytest.mark.parametrize("tokens,hidden,ffn", GEMM_SHAPES)
+def test_gemm_qkv_up(ptb_lib, tokens, hidden, ffn):
+    xn = workloads.normal_bf16((tokens, hidden), seed=3)
+    w_qkv = workloads.normal_bf16((3 * hidden, hidden), seed=4, std=1.0 / math.sqrt(hidden))
+    w_up = workloads.normal_bf16((ffn, hidden), seed=5, std=1.0 / math.sqrt(hidden))
+    u = ptb_lib.gemm_qkv_up(xn.cuda(), w_qkv.cuda(), w_up.cuda())
+    want = np.concatenate([oracle.linear(xn, w_qkv),
+                           oracle.gelu_tanh(oracle.linear(xn, w_up))], axis=1)
+    assert_close(u, want, f"GEMM1 {tokens}x{hidden}x{ffn}")
+
+
+# ------------------------------------------------- [out | down] GEMM + x --
+
+@pytest.mark.parametrize("tokens,hidden,ffn", GEMM_SHAPES)
+def test_gemm_out_down_residual(ptb_lib, tokens, hidden, ffn):
+    # ctx and g live as column blocks of one fused buffer, as in the layer.
+    ld = 3 * hidden + ffn
+    u = workloads.normal_bf16((tokens, ld), seed=6, std=0.5).cuda()
+    ctx, g = u[:, :hidden], u[:, 3 * hidden:]
+    w_o = workloads.normal_bf16((hidden, hidden), seed=7, std=1.0 / math.sqrt(hidden))
+    w_down = workloads.normal_bf16((hidden, ffn), seed=8, std=1.0 / math.sqrt(ffn))
+    x = workloads.normal_bf16((tokens, hidden), seed=9)
+    y = ptb_lib.gemm_out_down(ctx, g, w_o.cuda(), w_down.cuda(), x.cuda())
+    want = to_np(x) + oracle.linear(ctx.cpu(), w_o) + oracle.linear(g.cpu(), w_down)
+    assert_close(y, want, f"GEMM2 {tokens}x{hidden}x{ffn}")
+
+
+# --------------------------------------------------------------------- SWA --
+
+SWA_CASES = [  # batch, heads, seq, head_dim, window
+    (1, 1, 1, 64, 1), (1, 2, 63, 64, 5), (2, 3, 64, 64, 64), (1, 2, 65, 32, 64),
+    (2, 2, 200, 128, 17), (1, 4, 333, 96, 100), (1, 2, 257, 16, 1), (1, 2, 300, 64, 300),
+    (1, 1, 500, 128, 2000), (2, 2, 1000, 128, 129), (1, 2, 700, 96, 511), (1, 1, 130, 32, 2),
+]
+
+
+@pytest.mark.parametrize("b,h,s,d,w", SWA_CASES)
+def test_swa_matches_oracle_and_counts(ptb_lib, b, h, s, d, w):
+    q, k, v = workloads.swa_inputs(b, h, s, d, seed=s + w)
+    o, counts = ptb_lib.swa_attention_counts(q.cuda(), k.cuda(), v.cuda(), w)
+    assert_close(o, oracle.swa(q, k, v, w), f"SWA {b}x{h}x{s}x{d} w={w}")
+    want_counts = np.broadcast_to(oracle.attended_counts(s, w), (b, h, s))
+    assert np.array_equal(counts.cpu().numpy(), want_counts), "attended-key counts differ"
+    o_plain = ptb_lib.swa_attention(q.cuda(), k.cuda(), v.cuda(), w)
+    assert_close(o_plain, o, "SWA without counts", rel_l2=1e-6, max_abs=1e-6)
+
+
+@pytest.mark.parametrize("s,d,w", [(128, 128, 32), (300, 64, 64), (260, 32, 7), (200, 128, 1000)])
+def test_swa_mask_zero_pattern(ptb_lib, s, d, w):
+    """Q = K = 0 makes every in-band weight 1/count; V row j is the one-hot of
+    j mod d, so o[i, c] is nonzero exactly where a key j with j mod d = c is
+    in row i's window.  The zero pattern is compared bit for bit."""
+    z = torch.zeros(1, 1, s, d, dtype=torch.bfloat16)
+    v = torch.zeros(1, 1, s, d, dtype=torch.bfloat16)
+    v[0, 0, torch.arange(s), torch.arange(s) % d] = 1
+    o = ptb_lib.swa_attention(z.cuda(), z.cuda(), v.cuda(), w).cpu()
+    want = oracle.swa(z, z, v, w)
+    got = to_np(o)
+    assert np.array_equal(got == 0, want == 0), "mask zero pattern differs"
+    nz = want != 0
+    assert np.all(np.abs(got[nz] - want[nz]) <= 2.0 ** -8 * want[nz])
+
+
+@pytest.mark.parametrize("w", [512, 2048, 1])
+def test_swa_operator_config(ptb_lib, w):
+    """The SWA operator at batch 4, 16 heads, head_dim 128, seq 2048."""
+    cfg = workloads.SWA_CONFIGS["swa"]
+    q, k, v = workloads.swa_inputs(cfg.batch, cfg.heads, cfg.seq, cfg.head_dim, cfg.seed)
+    o, counts = ptb_lib.swa_attention_counts(q.cuda(), k.cuda(), v.cuda(), w)
+    o = o.cpu()
+    if w == 1:
+        assert torch.equal(o, v), "window 1 must return V exactly"
+    for bi in range(cfg.batch):
+        assert_close(o[bi], oracle.swa(q[bi], k[bi], v[bi], w), f"SWA op w={w} batch {bi}")
+    want_counts = np.broadcast_to(oracle.attended_counts(cfg.seq, w), counts.shape)
+    assert np.array_equal(counts.cpu().numpy(), want_counts)
+
+
+def test_swa_strided_in_place(ptb_lib):
+    """Q, K, V as head-strided column blocks of one [T, 3H + F] buffer and the
+    output written over Q, as the layer does."""
+    b, s, nh, d, f, w = 2, 300, 4, 64, 128, 77
+    hdim = nh * d
+    ld = 3 * hdim + f
+    u = workloads.normal_bf16((b, s, ld), seed=11).cuda()
+    view = lambda off: u[:, :, off:off + hdim].unflatten(2, (nh, d)).transpose(1, 2)  # noqa: E731
+    q, k, v = view(0), view(hdim), view(2 * hdim)
+    want = oracle.swa(q.cpu(), k.cpu(), v.cpu(), w)
+    untouched = u[:, :, hdim:].clone()
+    ptb_lib.swa_attention_strided(q, k, v, q, w)
+    assert_close(view(0), want, "strided in-place SWA")
+    assert torch.equal(u[:, :, hdim:], untouched), "SWA wrote outside its output block"
+
+
+# ---------------------------------------------------------------- PTB layer --
+
+SMALL_LAYERS = [
+    workloads.PTB_CONFIGS["tiny"],
+    workloads.PTB_CONFIGS["tiny"].with_window(128),
+    workloads.small_ptb(2, 300, 256, 4, 1024, 100, seed=21),
+    workloads.small_ptb(1, 257, 384, 4, 1536, 65, seed=22),
+    workloads.small_ptb(3, 130, 128, 8, 512, 1, seed=23),
+    workloads.small_ptb(1, 200, 512, 4, 2048, 1000, seed=24),
+    workloads.small_ptb(1, 1, 64, 2, 64, 5, seed=25),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL_LAYERS, ids=lambda c: c.name)
+@pytest.mark.parametrize("own_workspace", [False, True])
+def test_ptb_forward_small(ptb_lib, cfg, own_workspace):
+    host = workloads.ptb_inputs(cfg)
+    d = _cuda(host)
+    ws = None
+    if own_workspace:
+        n = ptb_lib.workspace_size(cfg.batch, cfg.seq, cfg.hidden, cfg.ffn)
+        ws = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")  # NaN-pattern canary
+    y = ptb_lib.ptb_forward(d["x"], d["ln_gamma"], d["ln_beta"], d["w_qkv"], d["w_o"], d["w_up"],
+                            d["w_down"], cfg.heads, cfg.window, workspace=ws)
+    want = oracle.ptb_forward(host["x"], host["ln_gamma"], host["ln_beta"], host["w_qkv"],
+                              host["w_o"], host["w_up"], host["w_down"], cfg.heads, cfg.window)
+    assert_close(y, want, cfg.name)
+
+
+def test_ptb_forward_deterministic_and_events(ptb_lib):
+    cfg = workloads.small_ptb(2, 300, 256, 4, 1024, 100, seed=21)
+    d = _cuda(workloads.ptb_inputs(cfg))
+    args = (d["x"], d["ln_gamma"], d["ln_beta"], d["w_qkv"], d["w_o"], d["w_up"], d["w_down"],
+            cfg.heads, cfg.window)
+    y0 = ptb_lib.ptb_forward(*args)
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    y1 = ptb_lib.ptb_forward_events(*args, events)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1)
+    for a, b in zip(events, events[1:]):
+        assert a.elapsed_time(b) >= 0.0
+
+
+def test_ptb_special_case_attention_off(ptb_lib):
+    """W_o = 0 leaves y = x + MLP(LN(x)); W_down = 0 leaves y = x + Attn(LN(x))."""
+    cfg = workloads.small_ptb(1, 200, 256, 4, 512, 33, seed=26)
+    host = workloads.ptb_inputs(cfg)
+    for zero in ("w_o", "w_down"):
+        h2 = dict(host)
+        h2[zero] = torch.zeros_like(host[zero])
+        d = _cuda(h2)
+        y = ptb_lib.ptb_forward(d["x"], d["ln_gamma"], d["ln_beta"], d["w_qkv"], d["w_o"],
+                                d["w_up"], d["w_down"], cfg.heads, cfg.window)
+        want = oracle.ptb_forward(h2["x"], h2["ln_gamma"], h2["ln_beta"], h2["w_qkv"], h2["w_o"],
+                                  h2["w_up"], h2["w_down"], cfg.heads, cfg.window)
+        assert_close(y, want, f"{zero} = 0")
+
+
+@pytest.mark.parametrize("name", ["13b", "175b", "530b"])
+def test_ptb_forward_full_size_sampled(ptb_lib, name):
+    """Full-size layers, launched exactly as the benchmark launches them
+    (caller workspace, current stream), checked on sampled rows."""
+    cfg = workloads.PTB_CONFIGS[name]
+    d = workloads.ptb_inputs(cfg, device="cuda")
+    ws = torch.empty(ptb_lib.workspace_size(cfg.batch, cfg.seq, cfg.hidden, cfg.ffn),
+                     dtype=torch.uint8, device="cuda")
+    y = ptb_lib.ptb_forward(d["x"], d["ln_gamma"], d["ln_beta"], d["w_qkv"], d["w_o"], d["w_up"],
+                            d["w_down"], cfg.heads, cfg.window, workspace=ws)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(y).all())
+    rows = workloads.sample_rows(cfg.seq, cfg.window)
+    host = {k: v.cpu() for k, v in d.items()}
+    del d, ws
+    want = oracle.ptb_forward(host["x"], host["ln_gamma"], host["ln_beta"], host["w_qkv"],
+                              host["w_o"], host["w_up"], host["w_down"], cfg.heads, cfg.window,
+                              rows=rows)
+    assert_close(y[:, rows], want, f"{name} sampled rows {rows}")
