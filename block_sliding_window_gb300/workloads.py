@@ -127,7 +127,9 @@ def sample_rows(seq: int, window: int) -> list:
 
 
 def small_ptb(batch: int, seq: int, hidden: int, heads: int, ffn: int,
-              window: int, seed: int, w_std: float = 0.05) -> PTBConfig:
-    """An ad-hoc layer shape for the tile-edge parity cases."""
+              window: int, seed: int, w_std: float = 0.02) -> PTBConfig:
+    """An ad-hoc layer shape for the tile-edge parity cases.  Weights use the
+    same N(0, 0.02^2) as the tiny and 13B-class workloads, which keeps |y|
+    below 8, where one bf16 ulp of the output is 2^-5."""
     return PTBConfig(f"b{batch}s{seq}h{hidden}n{heads}f{ffn}w{window}", batch,
                      seq, hidden, heads, ffn, window, w_std, seed)
