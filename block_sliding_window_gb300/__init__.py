@@ -151,6 +151,10 @@ def ptb_forward_events(x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, heads: in
         x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, heads, window, y, workspace)
     if len(events) != 5:
         raise ValueError("need 5 events")
+    st_obj = torch.cuda.current_stream() if stream is None else stream
+    for ev in events:
+        if not ev.cuda_event:  # torch creates the CUDA event on its first record
+            ev.record(st_obj)
     handles = (ctypes.c_void_p * 5)(*[ev.cuda_event for ev in events])
     st = lib.ptb_forward_events(_ptr(x), _ptr(ln_gamma), _ptr(ln_beta), _ptr(w_qkv), _ptr(w_o),
                                 _ptr(w_up), _ptr(w_down), batch, seq, hidden, ffn, heads, window,

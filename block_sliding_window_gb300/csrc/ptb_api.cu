@@ -251,6 +251,9 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
   for (const void* p : ptrs)
     if (!aligned(p, 16)) return PTB_ERR_ALIGN;
   if (events && n_events != 5) return PTB_ERR_ARG;
+  if (events)
+    for (int i = 0; i < 5; ++i)
+      if (!events[i]) return PTB_ERR_ARG;
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != PTB_OK) return st;
@@ -281,21 +284,24 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
   ptb_bf16* u = reinterpret_cast<ptb_bf16*>(static_cast<char*>(workspace) +
                                             round_up(tokens * hidden * 2, kAlign));
   const int64_t ldu = 3 * hidden + ffn;
-  auto mark = [&](int i) {
-    if (events) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream);
+  auto mark = [&](int i) -> bool {
+    if (!events) return true;
+    if (cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) == cudaSuccess) return true;
+    cudaGetLastError();  // the failed record must not be reported by a later launch
+    return false;
   };
 
   // 1. xn = LN(x)
-  mark(0);
+  if (!mark(0)) return PTB_ERR_ARG;
   if (launch_layernorm(bf(x), bf(ln_gamma), bf(ln_beta), tokens, static_cast<int>(hidden), 1e-5f,
                        bf(xn), stream) != cudaSuccess)
     return PTB_ERR_LAUNCH;
   // 2. U = [xn W_qkv^T | gelu(xn W_up^T)]
-  mark(1);
+  if (!mark(1)) return PTB_ERR_ARG;
   st = gemm_qkv_up(ds, xn, w_qkv, w_up, tokens, hidden, ffn, u, stream);
   if (st != PTB_OK) return st;
   // 3. ctx = SWA(Q, K, V), written over Q inside U
-  mark(2);
+  if (!mark(2)) return PTB_ERR_ARG;
   SwaArgs sa;
   std::memset(&sa, 0, sizeof(sa));
   sa.q = bf(u);
@@ -313,11 +319,11 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
   sa.scale_log2 = (1.0f / std::sqrt(static_cast<float>(d))) * 1.4426950408889634f;
   if (launch_swa(sa, stream) != cudaSuccess) return PTB_ERR_LAUNCH;
   // 4. y = x + [ctx | G] [W_o | W_down]^T
-  mark(3);
+  if (!mark(3)) return PTB_ERR_ARG;
   st = gemm_out_down(ds, u, ldu, u + 3 * hidden, ldu, w_o, w_down, x, tokens, hidden, ffn, y,
                      stream);
   if (st != PTB_OK) return st;
-  mark(4);
+  if (!mark(4)) return PTB_ERR_ARG;
   return PTB_OK;
 }
 

@@ -104,7 +104,8 @@ ptb_status ptb_forward(const ptb_bf16* x, const ptb_bf16* ln_gamma, const ptb_bf
  * Same as ptb_forward, and records `events[0..4]` (cudaEvent_t handles owned
  * by the caller; n_events must be 5) on `stream` before the LayerNorm, the
  * first GEMM, the attention, the second GEMM and after it, so a caller can
- * time each kernel.
+ * time each kernel.  Every handle must be a created event; a NULL handle or
+ * a failed record returns PTB_ERR_ARG (kernels already enqueued stay queued).
  */
 ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
                               const ptb_bf16* ln_beta, const ptb_bf16* w_qkv,

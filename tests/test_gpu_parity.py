@@ -105,7 +105,7 @@ def test_swa_matches_oracle_and_counts(ptb_lib, b, h, s, d, w):
     want_counts = np.broadcast_to(oracle.attended_counts(s, w), (b, h, s))
     assert np.array_equal(counts.cpu().numpy(), want_counts), "attended-key counts differ"
     o_plain = ptb_lib.swa_attention(q.cuda(), k.cuda(), v.cuda(), w)
-    assert_close(o_plain, o, "SWA without counts", rel_l2=1e-6, max_abs=1e-6)
+    assert torch.equal(o_plain, o), "the counting kernel must compute the same output"
 
 
 @pytest.mark.parametrize("s,d,w", [(128, 128, 32), (300, 64, 64), (260, 32, 7), (200, 128, 1000)])

@@ -1,0 +1,22 @@
+"""CPU checks of the tolerance helper used by the parity tests."""
+import numpy as np
+import torch
+
+from tests.parity import bf16_half_ulp, errors
+
+
+def test_half_ulp_values():
+    v = np.array([1.0, 1.5, 3.99, 4.0, 8.0, 9.27, 15.9, -8.5, 0.25])
+    want = np.array([2.0 ** -8, 2.0 ** -8, 2.0 ** -7, 2.0 ** -6, 2.0 ** -5, 2.0 ** -5,
+                     2.0 ** -5, 2.0 ** -5, 2.0 ** -10])
+    assert np.array_equal(bf16_half_ulp(v), want)
+    assert bf16_half_ulp(np.array([0.0]))[0] == 0.0
+
+
+def test_rounding_to_bf16_stays_within_half_ulp():
+    g = torch.Generator().manual_seed(0)
+    v = (torch.randn(200000, generator=g, dtype=torch.float32) * 6).double()  # fp32 values: one rounding
+    r = v.float().to(torch.bfloat16).double()
+    assert bool(((r - v).abs().numpy() <= bf16_half_ulp(v.numpy())).all())
+    rel, mx, ex = errors(r, v)
+    assert ex == 0.0 and mx > 0.03  # plain max-abs exceeds 3e-2 from rounding alone
