@@ -20,3 +20,23 @@ def test_rounding_to_bf16_stays_within_half_ulp():
     assert bool(((r - v).abs().numpy() <= bf16_half_ulp(v.numpy())).all())
     rel, mx, ex = errors(r, v)
     assert ex == 0.0 and mx > 0.03  # plain max-abs exceeds 3e-2 from rounding alone
+
+
+def test_bf16_storage_model_sane():
+    import oracle
+    from block_sliding_window_gb300 import workloads
+    from tests.bf16_storage_model import ptb_forward_bf16_storage
+    cfg = workloads.PTB_CONFIGS["tiny"]
+    h = workloads.ptb_inputs(cfg)
+    rows = workloads.sample_rows(cfg.seq, cfg.window)
+    args = (h["x"], h["ln_gamma"], h["ln_beta"], h["w_qkv"], h["w_o"], h["w_up"], h["w_down"],
+            cfg.heads, cfg.window)
+    want = oracle.ptb_forward(*args, rows=rows)[0]
+    model = ptb_forward_bf16_storage(*args, rows)
+    rel, mx, ex = errors(model, want)
+    assert 0 < rel < 1e-2 and ex < 1e-2
+    # zero weights: y = x exactly, through every storage point
+    z = {k: torch.zeros_like(h[k]) for k in ("w_qkv", "w_o", "w_up", "w_down")}
+    model0 = ptb_forward_bf16_storage(h["x"], h["ln_gamma"], h["ln_beta"], z["w_qkv"], z["w_o"],
+                                      z["w_up"], z["w_down"], cfg.heads, cfg.window, rows)
+    assert np.array_equal(model0, h["x"][0, rows].double().numpy())
