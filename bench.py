@@ -233,7 +233,7 @@ def run_reference(args, world, rank):
         return
     name = args.workload if args.workload != "swa" else "175b"
     cfg = workload_config(name)
-    rows = args.cpu_rows
+    rows = args.ref_rows
     f64 = oracle_sample(cfg, rows, seed_device="cuda" if torch.cuda.is_available() else "cpu")
     time_oracle(cfg, f64, rows, max(0, min(args.warmup, 1)))
     times = time_oracle(cfg, f64, rows, args.steps)
@@ -328,7 +328,7 @@ def run_ours(args, world, rank, local):
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local)  # sampled over the timed and the e2e regions
     barrier(world)
     torch.cuda.synchronize()
     t_start.record(stream)
@@ -337,7 +337,6 @@ def run_ours(args, world, rank, local):
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    clk = clocks.stop()
     status = bsw.last_device_error()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
@@ -370,6 +369,7 @@ def run_ours(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
+    clk = clocks.stop()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
 
     fl = layer_flops(cfg)
@@ -413,11 +413,14 @@ def run_ours(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["175b", "13b", "530b", "tiny", "swa"], default="175b")
-    ap.add_argument("--cpu-rows", type=int, default=32)
+    ap.add_argument("--cpu-rows", type=int, default=1024,
+                    help="rows of the layer the CPU baseline computes (about 10 s of oracle work)")
+    ap.add_argument("--ref-rows", type=int, default=64,
+                    help="rows per step of the reference arm (the oracle)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     world, rank, local = dist_setup()
