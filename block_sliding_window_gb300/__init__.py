@@ -39,6 +39,7 @@ SYMBOLS = {
     "ptb_forward": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p]),
     "ptb_forward_events": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p, _p, _i32]),
     "ptb_release_workspace": (_st, []),
+    "ptb_forward_noalloc": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p]),
     "swa_attention": (_st, [_p, _p, _p, _i64, _i32, _i64, _i32, _i32, _f32, _p, _p]),
     "swa_attention_strided": (_st, [_p, _i64, _i64, _i64] * 4 + [_i64, _i32, _i64, _i32, _i32, _f32, _p]),
     "swa_attention_counts": (_st, [_p, _p, _p, _i64, _i32, _i64, _i32, _i32, _f32, _p, _p, _p]),

@@ -115,6 +115,38 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
                               size_t workspace_bytes, ptb_stream stream, void* const* events,
                               int32_t n_events);
 
+/*
+ * ptb_forward_noalloc: ptb_forward for callers that cannot allocate device
+ * memory.  The paper has no counterpart; this is a deployment convenience.
+ *
+ * Programs that manage all device memory themselves (a framework's caching
+ * allocator, a server that reserves memory at start-up and must not call
+ * cudaMalloc later because it can stall the device or fail when memory is
+ * fragmented, a plug-in whose host forbids raw allocations) can neither let
+ * the library grow its arena nor always lend it a buffer.  This entry point
+ * takes the same inputs and output as ptb_forward but uses, as scratch, one
+ * fixed 64 MiB array compiled into the library, so it calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ *   - Size limit: ptb_forward_workspace_size(batch, seq, hidden, ffn) must
+ *     be <= 64 MiB (67108864 bytes); larger layers return PTB_ERR_WORKSPACE
+ *     without launching anything.
+ *   - The array takes 64 MiB of device memory on every GPU where the
+ *     library's code for this entry point is loaded, until the process exits.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, which keeps whatever the last call left
+ *     in it; nothing in it has to start at zero.  Calls whose work overlaps on
+ *     the GPU (other streams, other host threads) race on it: serialise them.
+ * Other arguments, shape rules and errors are those of ptb_forward.
+ */
+ptb_status ptb_forward_noalloc(const ptb_bf16* x, const ptb_bf16* ln_gamma,
+                               const ptb_bf16* ln_beta, const ptb_bf16* w_qkv,
+                               const ptb_bf16* w_o, const ptb_bf16* w_up, const ptb_bf16* w_down,
+                               int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,
+                               int32_t heads, int32_t window, ptb_bf16* y, ptb_stream stream);
+
 /* Frees the library's own workspace arena on the current device (if any). */
 ptb_status ptb_release_workspace(void);
 
