@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "PTBError", "load", "ptb_forward", "ptb_forward_events", "swa_attention",
     "swa_attention_strided", "swa_attention_counts", "layernorm", "gemm_qkv_up",
-    "gemm_out_down", "workspace_size", "release_workspace", "last_device_error",
+    "gemm_out_down", "gemm_workspace_size", "workspace_size", "release_workspace", "last_device_error",
     "wait_probe", "LIB_PATH", "SYMBOLS",
 ]
 
@@ -44,8 +44,10 @@ SYMBOLS = {
     "swa_attention_strided": (_st, [_p, _i64, _i64, _i64] * 4 + [_i64, _i32, _i64, _i32, _i32, _f32, _p]),
     "swa_attention_counts": (_st, [_p, _p, _p, _i64, _i32, _i64, _i32, _i32, _f32, _p, _p, _p]),
     "ptb_layernorm": (_st, [_p, _p, _p, _i64, _i64, _f32, _p, _p]),
-    "ptb_gemm_qkv_up": (_st, [_p, _p, _p, _i64, _i64, _i64, _p, _p]),
-    "ptb_gemm_out_down": (_st, [_p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p, _p]),
+    "ptb_gemm_workspace_size": (_sz, [_i64, _i64, _i64]),
+    "ptb_gemm_qkv_up": (_st, [_p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
+    "ptb_gemm_out_down": (_st, [_p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p, _p, _sz,
+                                _p]),
     "ptb_last_device_error": (_st, []),
     "ptb_wait_probe": (_st, [ctypes.c_uint64, _p]),
 }
@@ -224,28 +226,42 @@ def layernorm(x, gamma, beta, eps: float = 1e-5, out=None, stream=None):
     return out
 
 
-def gemm_qkv_up(xn, w_qkv, w_up, u=None, stream=None):
+def gemm_workspace_size(tokens: int, hidden: int, ffn: int) -> int:
+    return int(load().ptb_gemm_workspace_size(tokens, hidden, ffn))
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def gemm_qkv_up(xn, w_qkv, w_up, u=None, workspace=None, stream=None):
     """u = [xn w_qkv^T | gelu_tanh(xn w_up^T)] for xn [T, H]."""
     lib = load()
     tokens, hidden = xn.shape
     ffn = w_up.shape[0]
     if u is None:
         u = torch.empty(tokens, 3 * hidden + ffn, dtype=torch.bfloat16, device=xn.device)
+    ws, ws_bytes = _ws(workspace)
     st = lib.ptb_gemm_qkv_up(_ptr(xn), _ptr(w_qkv), _ptr(w_up), tokens, hidden, ffn, _ptr(u),
-                             _stream(stream))
+                             ws, ws_bytes, _stream(stream))
     _check(st, "ptb_gemm_qkv_up")
     return u
 
 
-def gemm_out_down(ctx, g, w_o, w_down, x, y=None, stream=None):
+def gemm_out_down(ctx, g, w_o, w_down, x, y=None, workspace=None, stream=None):
     """y = x + ctx w_o^T + g w_down^T (ctx, g may be row-strided views)."""
     lib = load()
     tokens, hidden = x.shape
     ffn = w_down.shape[1]
     if y is None:
         y = torch.empty_like(x)
+    ws, ws_bytes = _ws(workspace)
     st = lib.ptb_gemm_out_down(_ptr(ctx), ctx.stride(0), _ptr(g), g.stride(0), _ptr(w_o),
-                               _ptr(w_down), _ptr(x), tokens, hidden, ffn, _ptr(y),
+                               _ptr(w_down), _ptr(x), tokens, hidden, ffn, _ptr(y), ws, ws_bytes,
                                _stream(stream))
     _check(st, "ptb_gemm_out_down")
     return y

@@ -19,7 +19,18 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
 //               lanes 32*(w%4) .. +31, i.e. one output row per thread),
 //               GELU or residual add in fp32, bf16 stores.  The epilogue of
-//               tile i overlaps the main loop of tile i+1.
+//               one work unit overlaps the main loop of the next.
+//
+// Work units.  The tiles that fill whole waves (a multiple of the grid) are
+// processed whole, M-fastest, so the M tiles of one weight block run at the
+// same time and share it through L2.  The remaining R < grid tiles of the
+// last, partial wave are each split along K into S pieces (R*S <= grid), one
+// piece per otherwise idle CTA.  A piece writes its fp32 partial tile to the
+// workspace and bumps an arrival counter per 32-row quarter of the tile; the
+// epilogue warp that arrives last for a quarter sums the S partials of those
+// rows in piece order (so the bits do not depend on who finished) and runs
+// the epilogue for them.  Nothing ever waits on another CTA or another warp.
+//
 // Every mbarrier wait is bounded (see mbar_wait); on a timeout all roles
 // unwind, wait for their own copies and MMAs, free TMEM and return.
 #include "ptb_device.cuh"
@@ -47,6 +58,71 @@ __device__ __forceinline__ float gelu_tanh(float z) {
   const float k0 = 0.7978845608028654f;  // sqrt(2 / pi)
   const float k1 = 0.044715f;
   return 0.5f * z * (1.0f + tanhf(k0 * (z + k1 * z * z * z)));
+}
+
+// One unit of work: k-blocks [kb0, kb1) of one output tile.  slot >= 0 marks
+// a K piece of a remainder tile (its index in the partial-tile buffer).
+struct Unit {
+  int tile, kb0, kb1, slot;
+};
+
+// The i-th unit of this CTA; false when the CTA has no more work.
+__device__ __forceinline__ bool unit_at(const GemmArgs& p, int num_tiles, int num_kb, int i,
+                                        Unit& u) {
+  const int grid = gridDim.x;
+  if (p.split_s < 2) {
+    const int tile = blockIdx.x + i * grid;
+    if (tile >= num_tiles) return false;
+    u = {tile, 0, num_kb, -1};
+    return true;
+  }
+  const int whole = num_tiles - p.split_r;  // a multiple of grid
+  const int n_whole = whole / grid;
+  if (i < n_whole) {
+    u = {static_cast<int>(blockIdx.x) + i * grid, 0, num_kb, -1};
+    return true;
+  }
+  if (i == n_whole && static_cast<int>(blockIdx.x) < p.split_r * p.split_s) {
+    const int r = blockIdx.x / p.split_s;
+    const int s = blockIdx.x % p.split_s;
+    u = {whole + r, s * num_kb / p.split_s, (s + 1) * num_kb / p.split_s,
+         static_cast<int>(blockIdx.x)};
+    return true;
+  }
+  return false;
+}
+
+// Epilogue of one 32-column chunk of one output row: acc (fp32) -> out (bf16).
+template <int EPI>
+__device__ __forceinline__ void store_chunk(const GemmArgs& p, int row, int col,
+                                            const float (&acc)[32]) {
+  uint32_t packed[16];
+  if constexpr (EPI == kEpiQkvGelu) {
+    if (col >= p.gelu_col) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        packed[j] = pack_bf16x2(gelu_tanh(acc[2 * j]), gelu_tanh(acc[2 * j + 1]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
+    }
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(p.resid + row * p.ld_resid + col);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint4 x = __ldg(src + v);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = v * 8 + j * 2;
+        packed[v * 4 + j] = pack_bf16x2(acc[e] + bf16_lo(xs[j]), acc[e + 1] + bf16_hi(xs[j]));
+      }
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.ld_out + col);
+#pragma unroll
+  for (int v = 0; v < 4; ++v)
+    dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
 }
 
 template <int BN, int EPI>
@@ -112,12 +188,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       uint32_t armed = 0;  // bit s: stage s has had a load issued
       uint32_t armed_parity = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m0 = (tile % num_m) * BM;
-        const int n0 = (tile / num_m) * BN;
+      Unit u;
+      for (int i = 0; ok && unit_at(p, num_tiles, num_kb, i, u); ++i) {
+        const int m0 = (u.tile % num_m) * BM;
+        const int n0 = (u.tile / num_m) * BN;
         const bool nlo = n0 < p.n_split;
         const int by = nlo ? n0 : n0 - p.n_split;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
@@ -153,14 +230,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int local = 0;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
-        const int acc = local & 1;
-        const uint32_t acc_phase = (local >> 1) & 1;
+      Unit u;
+      for (int i = 0; ok && unit_at(p, num_tiles, num_kb, i, u); ++i) {
+        const int acc = i & 1;
+        const uint32_t acc_phase = (i >> 1) & 1;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status)) {
             ok = false;
             break;
@@ -172,7 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             // +32 bytes along K inside the swizzled row = +2 in the
             // descriptor's 16-byte address units.
-            umma_bf16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+            umma_bf16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                         (kb != u.kb0 || kk != 0) ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == C::kStages) {
@@ -190,60 +268,83 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   } else {
     // --------------------------------------------------------- epilogue --
     const int quarter = warp & 3;
-    int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
-      const int acc = local & 1;
-      const uint32_t acc_phase = (local >> 1) & 1;
-      if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status)) break;
+    const int row_local = quarter * 32 + lane;
+    Unit u;
+    for (int i = 0; unit_at(p, num_tiles, num_kb, i, u); ++i) {
+      const int acc_buf = i & 1;
+      const uint32_t acc_phase = (i >> 1) & 1;
+      if (!mbar_wait(&tfull_bar[acc_buf], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
-      const int m0 = (tile % num_m) * BM;
-      const int n0 = (tile / num_m) * BN;
-      const int row = m0 + quarter * 32 + lane;
-      const uint32_t t_row =
-          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      const int m0 = (u.tile % num_m) * BM;
+      const int n0 = (u.tile / num_m) * BN;
+      const int row = m0 + row_local;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc_buf * BN);
+      bool finish = true;
+      if (u.slot >= 0) {
+        // A K piece: publish the fp32 partial, then count the arrival.
+        float* mine = p.partials + (static_cast<int64_t>(u.slot) * BM + row_local) * BN;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + c, r);
-        tmem_ld_wait();
-        if (row < p.M) {
-          const int col = n0 + c;
-          uint32_t packed[16];
-          if constexpr (EPI == kEpiQkvGelu) {
-            if (col >= p.gelu_col) {
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + c, r);
+          tmem_ld_wait();
+          float4* dst = reinterpret_cast<float4*>(mine + c);
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                packed[j] = pack_bf16x2(gelu_tanh(__uint_as_float(r[2 * j])),
-                                        gelu_tanh(__uint_as_float(r[2 * j + 1])));
-            } else {
+          for (int v = 0; v < 8; ++v)
+            __stcg(dst + v, make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                        __uint_as_float(r[4 * v + 2]),
+                                        __uint_as_float(r[4 * v + 3])));
+        }
+        // Each warp owns its 32 rows: it counts its own arrival for that
+        // quarter of the tile, and the last warp to arrive for the quarter
+        // finishes those rows.  No warp waits for another.
+        __threadfence();
+        __syncwarp();
+        unsigned prev = 0;
+        if (lane == 0) prev = atomicAdd(p.counters + (u.slot / p.split_s) * 4 + quarter, 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        finish = prev == static_cast<unsigned>(p.split_s - 1);
+        if (finish) __threadfence();
+      }
+      if (finish && u.slot < 0) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + c, r);
+          tmem_ld_wait();
+          float acc[32];
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                packed[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-            }
-          } else {
-            const uint4* src = reinterpret_cast<const uint4*>(p.resid + row * p.ld_resid + col);
+          for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
+          if (row < p.M) store_chunk<EPI>(p, row, n0 + c, acc);
+        }
+      } else if (finish) {
+        // Sum every piece's partial (this warp's own included) in piece order,
+        // so the result does not depend on which warp happened to finish.
+        const int group0 = (u.slot / p.split_s) * p.split_s;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float acc[32];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint4 x = __ldg(src + v);
-              const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+          for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+          for (int s = 0; s < p.split_s; ++s) {
+            const float4* src = reinterpret_cast<const float4*>(
+                p.partials + (static_cast<int64_t>(group0 + s) * BM + row_local) * BN + c);
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int e = v * 8 + j * 2;
-                packed[v * 4 + j] = pack_bf16x2(__uint_as_float(r[e]) + bf16_lo(xs[j]),
-                                                __uint_as_float(r[e + 1]) + bf16_hi(xs[j]));
-              }
+            for (int v = 0; v < 8; ++v) {
+              const float4 q = __ldcg(src + v);
+              acc[4 * v] += q.x;
+              acc[4 * v + 1] += q.y;
+              acc[4 * v + 2] += q.z;
+              acc[4 * v + 3] += q.w;
             }
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.ld_out + col);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                packed[4 * v + 3]);
+          if (row < p.M) store_chunk<EPI>(p, row, n0 + c, acc);
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      if (lane == 0) mbar_arrive(&tempty_bar[acc_buf]);
     }
   }
 
@@ -275,7 +376,33 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+GemmPlan plan_gemm(int64_t tiles, int64_t num_kb, int sms, int block_n) {
+  GemmPlan g;
+  g.grid = static_cast<int>(tiles < sms ? tiles : sms);
+  g.split_r = 0;
+  g.split_s = 1;
+  // Remainder tiles of the last, partial wave (all tiles if fewer than SMs).
+  const int64_t r = tiles - (tiles / sms) * sms;
+  if (r > 0) {
+    int64_t s = sms / r;
+    const int64_t s_k = num_kb / kMinSplitKBlocks;  // each piece keeps >= kMinSplitKBlocks
+    if (s_k < s) s = s_k;
+    if (s >= 2) {
+      g.split_r = static_cast<int>(r);
+      g.split_s = static_cast<int>(s);
+      if (tiles < sms) g.grid = static_cast<int>(r * s);
+    }
+  }
+  g.partial_bytes = static_cast<size_t>(g.split_r) * g.split_s * BM * block_n * sizeof(float);
+  g.counter_bytes = static_cast<size_t>(g.split_r) * 4 * sizeof(unsigned);
+  return g;
+}
+
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
+  if (a.split_s >= 2 && a.split_r > 0) {
+    cudaError_t e = cudaMemsetAsync(a.counters, 0, a.split_r * 4 * sizeof(unsigned), stream);
+    if (e != cudaSuccess) return e;
+  }
   if (a.epilogue == kEpiQkvGelu) {
     switch (a.block_n) {
       case 256: return launch_typed<256, kEpiQkvGelu>(a, stream);

@@ -89,6 +89,65 @@ int pick_block_n(int64_t a, int64_t b) {
 
 ptb_status launch_status(cudaError_t e) { return e == cudaSuccess ? PTB_OK : PTB_ERR_LAUNCH; }
 
+// SM count of the current device, or an upper bound when there is none.
+int current_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+    return sms;
+  cudaGetLastError();
+  return 256;
+}
+
+// Split plans of the two GEMMs of one layer.
+struct LayerPlans {
+  GemmPlan g1, g2;
+  int bn1, bn2;
+};
+
+LayerPlans plan_layer(int64_t tokens, int64_t hidden, int64_t ffn, int sms) {
+  LayerPlans lp;
+  lp.bn1 = pick_block_n(3 * hidden, ffn);
+  lp.bn2 = pick_block_n(hidden, hidden);
+  const int64_t m_tiles = (tokens + 127) / 128;
+  lp.g1 = plan_gemm(m_tiles * ((3 * hidden + ffn) / (lp.bn1 ? lp.bn1 : 64)), hidden / 64, sms,
+                    lp.bn1 ? lp.bn1 : 64);
+  lp.g2 = plan_gemm(m_tiles * (hidden / (lp.bn2 ? lp.bn2 : 64)), (hidden + ffn) / 64, sms,
+                    lp.bn2 ? lp.bn2 : 64);
+  return lp;
+}
+
+size_t gemm_scratch_bytes(const GemmPlan& g) {
+  return round_up(g.partial_bytes, kAlign) + round_up(g.counter_bytes, kAlign);
+}
+
+size_t layer_gemm_scratch(int64_t tokens, int64_t hidden, int64_t ffn, int sms) {
+  const LayerPlans lp = plan_layer(tokens, hidden, ffn, sms);
+  const size_t a = gemm_scratch_bytes(lp.g1), b = gemm_scratch_bytes(lp.g2);
+  return a > b ? a : b;
+}
+
+// Fills the grid / split fields of a launch.  Without scratch (or with too
+// little) the GEMM runs unsplit.
+void apply_plan(GemmArgs& a, int64_t tiles, int64_t num_kb, int sms, void* scratch,
+                size_t scratch_bytes) {
+  GemmPlan g = plan_gemm(tiles, num_kb, sms, a.block_n);
+  if (g.split_s >= 2 && scratch && scratch_bytes >= gemm_scratch_bytes(g)) {
+    a.grid = g.grid;
+    a.split_r = g.split_r;
+    a.split_s = g.split_s;
+    a.partials = static_cast<float*>(scratch);
+    a.counters = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) +
+                                             round_up(g.partial_bytes, kAlign));
+  } else {
+    a.grid = static_cast<int>(tiles < sms ? tiles : sms);
+    a.split_r = 0;
+    a.split_s = 1;
+    a.partials = nullptr;
+    a.counters = nullptr;
+  }
+}
+
 const __nv_bfloat16* bf(const ptb_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
 __nv_bfloat16* bf(ptb_bf16* p) { return reinterpret_cast<__nv_bfloat16*>(p); }
 
@@ -96,7 +155,7 @@ bool head_dim_ok(int64_t d) { return d == 16 || d == 32 || d == 64 || d == 96 ||
 
 ptb_status gemm_qkv_up(DeviceState* ds, const ptb_bf16* xn, const ptb_bf16* w_qkv,
                        const ptb_bf16* w_up, int64_t tokens, int64_t hidden, int64_t ffn,
-                       ptb_bf16* u, cudaStream_t stream) {
+                       ptb_bf16* u, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.block_n = pick_block_n(3 * hidden, ffn);
@@ -117,7 +176,7 @@ ptb_status gemm_qkv_up(DeviceState* ds, const ptb_bf16* xn, const ptb_bf16* w_qk
   a.gelu_col = static_cast<int>(3 * hidden);
   a.epilogue = kEpiQkvGelu;
   const int64_t tiles = (tokens + 127) / 128 * (n / a.block_n);
-  a.grid = static_cast<int>(tiles < ds->sms ? tiles : ds->sms);
+  apply_plan(a, tiles, hidden / 64, ds->sms, scratch, scratch_bytes);
   a.status = ds->status;
   return launch_status(launch_gemm(a, stream));
 }
@@ -125,7 +184,7 @@ ptb_status gemm_qkv_up(DeviceState* ds, const ptb_bf16* xn, const ptb_bf16* w_qk
 ptb_status gemm_out_down(DeviceState* ds, const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16* g,
                          int64_t ld_g, const ptb_bf16* w_o, const ptb_bf16* w_down,
                          const ptb_bf16* x, int64_t tokens, int64_t hidden, int64_t ffn,
-                         ptb_bf16* y, cudaStream_t stream) {
+                         ptb_bf16* y, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.block_n = pick_block_n(hidden, hidden);
@@ -147,7 +206,7 @@ ptb_status gemm_out_down(DeviceState* ds, const ptb_bf16* ctx, int64_t ld_ctx, c
   a.gelu_col = a.N;
   a.epilogue = kEpiResidual;
   const int64_t tiles = (tokens + 127) / 128 * (hidden / a.block_n);
-  a.grid = static_cast<int>(tiles < ds->sms ? tiles : ds->sms);
+  apply_plan(a, tiles, (hidden + ffn) / 64, ds->sms, scratch, scratch_bytes);
   a.status = ds->status;
   return launch_status(launch_gemm(a, stream));
 }
@@ -228,7 +287,15 @@ const char* ptb_status_string(ptb_status s) {
 size_t ptb_forward_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn) {
   if (batch < 1 || seq < 1 || hidden < 1 || ffn < 1) return 0;
   const size_t t = static_cast<size_t>(batch) * static_cast<size_t>(seq);
-  return round_up(t * hidden * 2, kAlign) + round_up(t * (3 * hidden + ffn) * 2, kAlign);
+  size_t gemm = 0;
+  if (hidden % 64 == 0 && ffn % 64 == 0)
+    gemm = layer_gemm_scratch(static_cast<int64_t>(t), hidden, ffn, current_sms());
+  return round_up(t * hidden * 2, kAlign) + round_up(t * (3 * hidden + ffn) * 2, kAlign) + gemm;
+}
+
+size_t ptb_gemm_workspace_size(int64_t tokens, int64_t hidden, int64_t ffn) {
+  if (tokens < 1 || hidden < 64 || ffn < 64 || hidden % 64 || ffn % 64) return 0;
+  return layer_gemm_scratch(tokens, hidden, ffn, current_sms());
 }
 
 ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
@@ -283,6 +350,9 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
   ptb_bf16* xn = static_cast<ptb_bf16*>(workspace);
   ptb_bf16* u = reinterpret_cast<ptb_bf16*>(static_cast<char*>(workspace) +
                                             round_up(tokens * hidden * 2, kAlign));
+  char* gemm_scratch = reinterpret_cast<char*>(u) + round_up(tokens * (3 * hidden + ffn) * 2, kAlign);
+  const size_t gemm_scratch_size =
+      need - static_cast<size_t>(gemm_scratch - static_cast<char*>(workspace));
   const int64_t ldu = 3 * hidden + ffn;
   auto mark = [&](int i) -> bool {
     if (!events) return true;
@@ -298,7 +368,8 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
     return PTB_ERR_LAUNCH;
   // 2. U = [xn W_qkv^T | gelu(xn W_up^T)]
   if (!mark(1)) return PTB_ERR_ARG;
-  st = gemm_qkv_up(ds, xn, w_qkv, w_up, tokens, hidden, ffn, u, stream);
+  st = gemm_qkv_up(ds, xn, w_qkv, w_up, tokens, hidden, ffn, u, gemm_scratch, gemm_scratch_size,
+                   stream);
   if (st != PTB_OK) return st;
   // 3. ctx = SWA(Q, K, V), written over Q inside U
   if (!mark(2)) return PTB_ERR_ARG;
@@ -321,7 +392,7 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
   // 4. y = x + [ctx | G] [W_o | W_down]^T
   if (!mark(3)) return PTB_ERR_ARG;
   st = gemm_out_down(ds, u, ldu, u + 3 * hidden, ldu, w_o, w_down, x, tokens, hidden, ffn, y,
-                     stream);
+                     gemm_scratch, gemm_scratch_size, stream);
   if (st != PTB_OK) return st;
   if (!mark(4)) return PTB_ERR_ARG;
   return PTB_OK;
@@ -432,7 +503,7 @@ ptb_status ptb_layernorm(const ptb_bf16* x, const ptb_bf16* gamma, const ptb_bf1
 
 ptb_status ptb_gemm_qkv_up(const ptb_bf16* xn, const ptb_bf16* w_qkv, const ptb_bf16* w_up,
                            int64_t tokens, int64_t hidden, int64_t ffn, ptb_bf16* u,
-                           ptb_stream stream) {
+                           void* workspace, size_t workspace_bytes, ptb_stream stream) {
   if (!xn || !w_qkv || !w_up || !u) return PTB_ERR_ARG;
   ptb_status st = check_gemm_shape(tokens, hidden, ffn);
   if (st != PTB_OK) return st;
@@ -441,14 +512,15 @@ ptb_status ptb_gemm_qkv_up(const ptb_bf16* xn, const ptb_bf16* w_qkv, const ptb_
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != PTB_OK) return st;
-  return gemm_qkv_up(ds, xn, w_qkv, w_up, tokens, hidden, ffn, u,
+  if (workspace && !aligned(workspace, kAlign)) return PTB_ERR_ALIGN;
+  return gemm_qkv_up(ds, xn, w_qkv, w_up, tokens, hidden, ffn, u, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream));
 }
 
 ptb_status ptb_gemm_out_down(const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16* g, int64_t ld_g,
                              const ptb_bf16* w_o, const ptb_bf16* w_down, const ptb_bf16* x,
                              int64_t tokens, int64_t hidden, int64_t ffn, ptb_bf16* y,
-                             ptb_stream stream) {
+                             void* workspace, size_t workspace_bytes, ptb_stream stream) {
   if (!ctx || !g || !w_o || !w_down || !x || !y) return PTB_ERR_ARG;
   ptb_status st = check_gemm_shape(tokens, hidden, ffn);
   if (st != PTB_OK) return st;
@@ -460,8 +532,9 @@ ptb_status ptb_gemm_out_down(const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != PTB_OK) return st;
-  return gemm_out_down(ds, ctx, ld_ctx, g, ld_g, w_o, w_down, x, tokens, hidden, ffn, y,
-                       static_cast<cudaStream_t>(stream));
+  if (workspace && !aligned(workspace, kAlign)) return PTB_ERR_ALIGN;
+  return gemm_out_down(ds, ctx, ld_ctx, g, ld_g, w_o, w_down, x, tokens, hidden, ffn, y, workspace,
+                       workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 ptb_status ptb_last_device_error(void) {

@@ -35,7 +35,25 @@ struct GemmArgs {
   int epilogue;
   int grid;  // persistent CTAs (<= number of SMs)
   unsigned* status;
+  // K split of the last, partial wave (split_s < 2: no split).
+  int split_r;          // remainder tiles that are split
+  int split_s;          // pieces per remainder tile
+  float* partials;      // [split_r * split_s][128][block_n] fp32
+  unsigned* counters;   // [split_r][4] arrival counters, zeroed before each launch
 };
+
+// Each K piece of a split tile keeps at least this many 64-wide k-blocks.
+constexpr int kMinSplitKBlocks = 8;
+
+struct GemmPlan {
+  int grid, split_r, split_s;
+  size_t partial_bytes, counter_bytes;
+};
+
+// Grid and K split for `tiles` output tiles of `num_kb` k-blocks on `sms`
+// SMs: whole waves of tiles, then the remainder tiles split along K over the
+// SMs the last wave would leave idle.
+GemmPlan plan_gemm(int64_t tiles, int64_t num_kb, int sms, int block_n);
 
 struct SwaArgs {
   const __nv_bfloat16 *q, *k, *v;

@@ -62,9 +62,11 @@ typedef enum {
 const char* ptb_status_string(ptb_status status);
 
 /*
- * Bytes of scratch that ptb_forward needs for this shape: the normalised
- * activations xn [T, H] and the fused projection output U [T, 3H + F]
- * (T = batch * seq), each bf16 and 256-byte aligned.
+ * Bytes of scratch that ptb_forward needs for this shape on the current
+ * device: the normalised activations xn [T, H] and the fused projection
+ * output U [T, 3H + F] (T = batch * seq), each bf16 and 256-byte aligned,
+ * followed by ptb_gemm_workspace_size(T, hidden, ffn) bytes for the GEMMs'
+ * split last wave.  The last part depends on the device's SM count.
  */
 size_t ptb_forward_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn);
 
@@ -199,26 +201,39 @@ ptb_status ptb_layernorm(const ptb_bf16* x, const ptb_bf16* gamma, const ptb_bf1
                          ptb_stream stream);
 
 /*
+ * Scratch (bytes) with which either GEMM below can split the tiles of its
+ * last, partial wave along K over the SMs that wave would leave idle: fp32
+ * partial tiles plus arrival counters (the counters are cleared on the
+ * stream before every launch).  Depends on the current device's SM count;
+ * 0 when no split applies.
+ */
+size_t ptb_gemm_workspace_size(int64_t tokens, int64_t hidden, int64_t ffn);
+
+/*
  * ptb_gemm_qkv_up: the fused first projection of the PTB,
  *   u[:, 0:3H]      = xn w_qkv^T
  *   u[:, 3H:3H+F]   = gelu_tanh(xn w_up^T)
  * xn [T, H], u [T, 3H+F] row-major bf16; H, F multiples of 64.
+ * workspace: NULL, or >= ptb_gemm_workspace_size() bytes (256-byte aligned)
+ * to let the last wave split along K; results are the same either way up to
+ * fp32 summation order.
  */
 ptb_status ptb_gemm_qkv_up(const ptb_bf16* xn, const ptb_bf16* w_qkv, const ptb_bf16* w_up,
                            int64_t tokens, int64_t hidden, int64_t ffn, ptb_bf16* u,
-                           ptb_stream stream);
+                           void* workspace, size_t workspace_bytes, ptb_stream stream);
 
 /*
  * ptb_gemm_out_down: the fused output projection with the residual,
  *   y = x + ctx w_o^T + g w_down^T,
  * one GEMM over the concatenated inner dimension [ctx | g] (H + F).
  * ctx [T, H] with row stride ld_ctx, g [T, F] with row stride ld_g (strides
- * in elements, multiples of 8), x and y [T, H] contiguous.
+ * in elements, multiples of 8), x and y [T, H] contiguous.  workspace as
+ * for ptb_gemm_qkv_up.
  */
 ptb_status ptb_gemm_out_down(const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16* g, int64_t ld_g,
                              const ptb_bf16* w_o, const ptb_bf16* w_down, const ptb_bf16* x,
                              int64_t tokens, int64_t hidden, int64_t ffn, ptb_bf16* y,
-                             ptb_stream stream);
+                             void* workspace, size_t workspace_bytes, ptb_stream stream);
 
 /*
  * Synchronises the current device, then returns and clears the device

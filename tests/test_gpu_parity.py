@@ -62,12 +62,20 @@ GEMM_SHAPES = [(128, 64, 256), (600, 256, 1024), (257, 384, 1536), (1, 64, 64),
                (2048, 1024, 4096), (333, 192, 320)]
 
 
+def _gemm_ws(ptb_lib, split, tokens, hidden, ffn):
+    """Scratch that lets the GEMM split its last wave along K (None: unsplit)."""
+    n = ptb_lib.gemm_workspace_size(tokens, hidden, ffn) if split else 0
+    return torch.full((n,), 0x7F, dtype=torch.uint8, device="cuda") if n else None
+
+
+@pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("tokens,hidden,ffn", GEMM_SHAPES)
-def test_gemm_qkv_up(ptb_lib, tokens, hidden, ffn):
+def test_gemm_qkv_up(ptb_lib, tokens, hidden, ffn, split):
     xn = workloads.normal_bf16((tokens, hidden), seed=3)
     w_qkv = workloads.normal_bf16((3 * hidden, hidden), seed=4, std=1.0 / math.sqrt(hidden))
     w_up = workloads.normal_bf16((ffn, hidden), seed=5, std=1.0 / math.sqrt(hidden))
-    u = ptb_lib.gemm_qkv_up(xn.cuda(), w_qkv.cuda(), w_up.cuda())
+    u = ptb_lib.gemm_qkv_up(xn.cuda(), w_qkv.cuda(), w_up.cuda(),
+                            workspace=_gemm_ws(ptb_lib, split, tokens, hidden, ffn))
     want = np.concatenate([oracle.linear(xn, w_qkv),
                            oracle.gelu_tanh(oracle.linear(xn, w_up))], axis=1)
     assert_close(u, want, f"GEMM1 {tokens}x{hidden}x{ffn}")
@@ -75,8 +83,9 @@ def test_gemm_qkv_up(ptb_lib, tokens, hidden, ffn):
 
 # ------------------------------------------------- [out | down] GEMM + x --
 
+@pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("tokens,hidden,ffn", GEMM_SHAPES)
-def test_gemm_out_down_residual(ptb_lib, tokens, hidden, ffn):
+def test_gemm_out_down_residual(ptb_lib, tokens, hidden, ffn, split):
     # ctx and g live as column blocks of one fused buffer, as in the layer.
     ld = 3 * hidden + ffn
     u = workloads.normal_bf16((tokens, ld), seed=6, std=0.5).cuda()
@@ -84,7 +93,8 @@ def test_gemm_out_down_residual(ptb_lib, tokens, hidden, ffn):
     w_o = workloads.normal_bf16((hidden, hidden), seed=7, std=1.0 / math.sqrt(hidden))
     w_down = workloads.normal_bf16((hidden, ffn), seed=8, std=1.0 / math.sqrt(ffn))
     x = workloads.normal_bf16((tokens, hidden), seed=9)
-    y = ptb_lib.gemm_out_down(ctx, g, w_o.cuda(), w_down.cuda(), x.cuda())
+    y = ptb_lib.gemm_out_down(ctx, g, w_o.cuda(), w_down.cuda(), x.cuda(),
+                              workspace=_gemm_ws(ptb_lib, split, tokens, hidden, ffn))
     want = to_np(x) + oracle.linear(ctx.cpu(), w_o) + oracle.linear(g.cpu(), w_down)
     assert_close(y, want, f"GEMM2 {tokens}x{hidden}x{ffn}")
 
@@ -197,6 +207,21 @@ def test_ptb_forward_deterministic_and_events(ptb_lib):
     assert torch.equal(y0, y1)
     for a, b in zip(events, events[1:]):
         assert a.elapsed_time(b) >= 0.0
+
+
+def test_gemm_split_repeatable(ptb_lib):
+    """The split last wave gives the same bits call after call (the arrival
+    order of the pieces does not change the summation order)."""
+    tokens, hidden, ffn = 2048, 1024, 4096
+    assert ptb_lib.gemm_workspace_size(tokens, hidden, ffn) > 0
+    u = workloads.normal_bf16((tokens, 3 * hidden + ffn), seed=12, std=0.5).cuda()
+    w_o = workloads.normal_bf16((hidden, hidden), seed=13, std=0.03).cuda()
+    w_down = workloads.normal_bf16((hidden, ffn), seed=14, std=0.015).cuda()
+    x = workloads.normal_bf16((tokens, hidden), seed=15).cuda()
+    ws = _gemm_ws(ptb_lib, True, tokens, hidden, ffn)
+    outs = [ptb_lib.gemm_out_down(u[:, :hidden], u[:, 3 * hidden:], w_o, w_down, x, workspace=ws)
+            for _ in range(3)]
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
 
 
 def test_ptb_special_case_attention_off(ptb_lib):

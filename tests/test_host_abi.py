@@ -52,8 +52,19 @@ def test_workspace_size(lib):
     t, h, f = 2 * 300, 256, 1024
     ws = lib.ptb_forward_workspace_size(2, 300, h, f)
     rnd = lambda v: (v + 255) // 256 * 256  # noqa: E731
-    assert ws == rnd(t * h * 2) + rnd(t * (3 * h + f) * 2)
+    assert ws == rnd(t * h * 2) + rnd(t * (3 * h + f) * 2) + lib.ptb_gemm_workspace_size(t, h, f)
     assert lib.ptb_forward_workspace_size(0, 300, h, f) == 0
+    assert lib.ptb_gemm_workspace_size(t, 100, f) == 0
+
+
+def test_gemm_split_plan_sizes(lib):
+    # Without a device the plan assumes 256 SMs.  175B shape: [out | down] has 768 tiles of
+    # 128 x 256 = 3 whole waves and [QKV | up] 5376 = 21 whole waves: no remainder to split.
+    assert lib.ptb_gemm_workspace_size(2048, 12288, 49152) == 0
+    # 2048 tokens, H = 1024, F = 4096: [out | down] has 16 x 4 = 64 tiles < 256 SMs,
+    # split into min(256 // 64, 80 // 8) = 4 pieces: 64 * 4 partial tiles of 128 x 256
+    # fp32 plus 64 x 4 counters.
+    assert lib.ptb_gemm_workspace_size(2048, 1024, 4096) == 64 * 4 * 128 * 256 * 4 + 1024
 
 
 FAKE = 1 << 20  # a 16-byte aligned non-null value; never dereferenced on the host
@@ -109,12 +120,12 @@ def test_swa_rejects_aliasing_and_misalignment(lib):
 
 
 def test_gemm_and_layernorm_checks(lib):
-    assert lib.ptb_gemm_qkv_up(FAKE, FAKE, FAKE, 128, 100, 256, FAKE, None) == 2
-    assert lib.ptb_gemm_qkv_up(None, FAKE, FAKE, 128, 64, 256, FAKE, None) == 1
+    assert lib.ptb_gemm_qkv_up(FAKE, FAKE, FAKE, 128, 100, 256, FAKE, None, 0, None) == 2
+    assert lib.ptb_gemm_qkv_up(None, FAKE, FAKE, 128, 64, 256, FAKE, None, 0, None) == 1
     assert lib.ptb_gemm_out_down(FAKE, 60, FAKE, 256, FAKE, FAKE, FAKE, 128, 64, 256, FAKE,
-                                 None) == 1
+                                 None, 0, None) == 1
     assert lib.ptb_gemm_out_down(FAKE, 68, FAKE, 256, FAKE, FAKE, FAKE, 128, 64, 256, FAKE,
-                                 None) == 3
+                                 None, 0, None) == 3
     assert lib.ptb_layernorm(FAKE, FAKE, FAKE, 4, 65536, 1e-5, FAKE, None) == 2
     assert lib.ptb_layernorm(FAKE, FAKE, FAKE, 4, 12, 1e-5, FAKE, None) == 2
     assert lib.ptb_wait_probe(0, None) == 1
