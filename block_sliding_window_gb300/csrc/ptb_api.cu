@@ -236,6 +236,7 @@ ptb_status swa_impl(const SwaArgs& in, float scale, cudaStream_t stream) {
   SwaArgs a = in;
   const float sc = scale == 0.f ? 1.0f / std::sqrt(static_cast<float>(in.head_dim)) : scale;
   a.scale_log2 = sc * 1.4426950408889634f;
+  a.status = ds->status;
   return launch_status(launch_swa(a, stream));
 }
 
@@ -257,6 +258,23 @@ __global__ void wait_probe_kernel(uint64_t limit_ns, unsigned* status) {
 }
 
 }  // namespace
+
+bool make_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box) {
+  if (!g_encode || rank < 1 || rank > 5) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) st[i] = strides_bytes[i];
+  }
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, b, e,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t launch_wait_probe(uint64_t limit_ns, unsigned* status, cudaStream_t stream) {
   wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
@@ -388,6 +406,7 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
   sa.head_dim = static_cast<int>(d);
   sa.window = window;
   sa.scale_log2 = (1.0f / std::sqrt(static_cast<float>(d))) * 1.4426950408889634f;
+  sa.status = ds->status;
   if (launch_swa(sa, stream) != cudaSuccess) return PTB_ERR_LAUNCH;
   // 4. y = x + [ctx | G] [W_o | W_down]^T
   if (!mark(3)) return PTB_ERR_ARG;

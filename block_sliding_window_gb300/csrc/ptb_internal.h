@@ -62,7 +62,14 @@ struct SwaArgs {
   int batch, heads, seq, head_dim, window;
   float scale_log2;  // softmax scale * log2(e)
   int* counts;       // optional per-row attended-key counts
+  unsigned* status;  // device status word (bounded waits record timeouts here)
 };
+
+// Encodes a bf16 tiled tensor map with 128-byte swizzle (rank <= 5; dims and
+// strides innermost first, strides in bytes for dims 1..rank-1).  Needs the
+// driver entry point, which the per-device set-up of the C ABI loads.
+bool make_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box);
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
 cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* gamma,
