@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     for (int i = 0; unit_at(p, num_tiles, num_kb, i, u); ++i) {
       const int acc_buf = i & 1;
       const uint32_t acc_phase = (i >> 1) & 1;
-      if (!mbar_wait(&tfull_bar[acc_buf], acc_phase, abort_flag, p.status)) break;
+      if (!mbar_wait_warp(&tfull_bar[acc_buf], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
       const int m0 = (u.tile % num_m) * BM;
       const int n0 = (u.tile / num_m) * BN;

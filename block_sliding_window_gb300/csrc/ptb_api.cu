@@ -237,6 +237,7 @@ ptb_status swa_impl(const SwaArgs& in, float scale, cudaStream_t stream) {
   const float sc = scale == 0.f ? 1.0f / std::sqrt(static_cast<float>(in.head_dim)) : scale;
   a.scale_log2 = sc * 1.4426950408889634f;
   a.status = ds->status;
+  a.sms = ds->sms;
   return launch_status(launch_swa(a, stream));
 }
 
@@ -407,6 +408,7 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
   sa.window = window;
   sa.scale_log2 = (1.0f / std::sqrt(static_cast<float>(d))) * 1.4426950408889634f;
   sa.status = ds->status;
+  sa.sms = ds->sms;
   if (launch_swa(sa, stream) != cudaSuccess) return PTB_ERR_LAUNCH;
   // 4. y = x + [ctx | G] [W_o | W_down]^T
   if (!mark(3)) return PTB_ERR_ARG;

@@ -63,6 +63,7 @@ struct SwaArgs {
   float scale_log2;  // softmax scale * log2(e)
   int* counts;       // optional per-row attended-key counts
   unsigned* status;  // device status word (bounded waits record timeouts here)
+  int sms;           // SMs of the device (persistent grid size)
 };
 
 // Encodes a bf16 tiled tensor map with 128-byte swizzle (rank <= 5; dims and

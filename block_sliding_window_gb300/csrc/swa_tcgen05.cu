@@ -6,24 +6,32 @@
 // FlashAttention-2 is the fused attention operator the notes list (§2.5,
 // Table 3).  Row i attends to keys max(0, i-w+1) .. i (causal, self-inclusive).
 //
-// One CTA per (128-query tile, head, batch entry), 192 threads:
-//   warp 0      TMA: the Q tile once, then the 64-key K and V tiles that
-//               intersect the band [q0 - w + 1, q0 + 127] (diagonal tile
-//               first) into a 3-stage ring.  d < 128 is read as 64-wide
-//               boxes; columns past d are zero-filled by TMA.
-//   warp 1      owns TMEM; one thread issues tcgen05.mma:
-//                 S_j  = Q K_j^T       (M 128, N 64, K d)   -> TMEM, 2 buffers
-//                 PV_j = P_j V_j       (M 128, N d, K 64)   -> TMEM, 2 buffers
-//               in the order S_0, S_1, PV_0, S_2, PV_1, ... so the softmax of
-//               one tile overlaps the tensor work of its neighbours.  V is
-//               used in place as an MN-major operand.
-//   warps 2..5  one query row per thread (TMEM lane = row): read the row of
-//               S_j, mask only on tiles that cross the band's edges, online
-//               softmax in the log2 domain (running max m and sum l in
-//               registers; no cross-thread reductions), write the bf16 row of
-//               P_j into shared memory in the 128-byte-swizzled layout the
-//               MMA reads, then fold PV_j into the fp32 output row kept in
-//               registers: O = O * alpha_j + PV_j.  Finally O / l -> bf16.
+// Persistent kernel: one CTA per SM walks work items = (256-query block,
+// head, batch entry).  An item is two 128-row query tiles X = 0, 1 that share
+// every K/V tile.  320 threads:
+//   warp 0      TMA: the two Q tiles of an item, then the 64-key K and V
+//               tiles intersecting the item's band [q0 - w + 1, q0 + 255]
+//               (diagonal tile first) into a 3-stage ring that runs on
+//               across items, with the tiles four positions ahead (and the
+//               next item's Q) prefetched into L2 so that ring loads do not
+//               pay DRAM latency.  d < 128 is read as 64-wide boxes;
+//               columns past d are zero-filled by TMA.
+//   warp 1      owns TMEM (512 columns: per query tile two 64-column score
+//               buffers and a d-column output accumulator); one thread issues
+//                 S_X = Q_X K_j^T   (M 128, N 64, K d)
+//                 O_X += P_X V_j    (M 128, N d, K 64; V read in place as an
+//                                    MN-major operand)
+//               skipping any (tile, X) pair that lies wholly outside the band.
+//   warps 2..9  two softmax warpgroups, one per query tile, one query row per
+//               thread (TMEM lane = row).  Per tile: read the score row, mask
+//               only on band-edge tiles, exponentiate in the log2 domain
+//               against a reference max that is raised only when the row max
+//               exceeds it by more than 8 (so P <= 2^8 in bf16); raising it
+//               rescales the running sum and the output row in TMEM.  The
+//               bf16 P row goes to shared memory (two buffers per query tile)
+//               in the 128-byte-swizzled operand layout, so a softmax warp
+//               never waits for a P V except to reuse a buffer two tiles old
+//               or to rescale O.  At the end of an item O / l -> bf16.
 // Every mbarrier wait is bounded (see mbar_wait); on a timeout all roles
 // unwind, wait for their own copies and MMAs, free TMEM and return.
 #include "ptb_device.cuh"
@@ -31,37 +39,78 @@
 namespace ptb {
 namespace {
 
-constexpr int BQ = 128;  // query rows per CTA (= MMA M)
-constexpr int BKV = 64;  // keys per K/V tile (= MMA N of S, K of PV)
-constexpr int NS = 3;    // K/V stages
-constexpr int kThreads = 192;
+constexpr int BQ = 128;       // rows per query tile (= MMA M)
+constexpr int QT = 2;         // query tiles per work item
+constexpr int BKV = 64;       // keys per K/V tile (= MMA N of S, K of PV)
+constexpr int NS = 3;         // K/V stages
+constexpr int kThreads = 320;
+constexpr float kRescaleLog2 = 8.0f;  // raise the reference max only past 2^8
+constexpr int kPrefetch = 4;          // K/V tiles prefetched into L2 ahead of the ring
 
 template <int D>
 struct SwaCfg {
-  static constexpr int kAtoms = (D + 63) / 64;     // 64-wide column blocks of d
-  static constexpr int kQBytes = kAtoms * BQ * 128;
-  static constexpr int kKVBytes = kAtoms * BKV * 128;  // one of K or V, one stage
-  static constexpr int kPBytes = BQ * BKV * 2;        // one P buffer
-  static constexpr int kSmemBytes = kQBytes + NS * 2 * kKVBytes + 2 * kPBytes + 256 + 1024;
-  static constexpr int kTmemS = 0;                    // 2 x 64 columns
-  static constexpr int kTmemPV = 2 * BKV;             // 2 x D columns
-  static constexpr int kTmemCols = (2 * BKV + 2 * D) <= 256 ? 256 : 512;
+  static constexpr int kAtoms = (D + 63) / 64;          // 64-wide column blocks of d
+  static constexpr int kQTileBytes = kAtoms * BQ * 128;
+  static constexpr int kKVBytes = kAtoms * BKV * 128;   // one of K or V, one stage
+  static constexpr int kPBytes = BQ * BKV * 2;          // P of one query tile
+  static constexpr int kSmemBytes =
+      QT * kQTileBytes + NS * 2 * kKVBytes + QT * 2 * kPBytes + 512 + 1024;
+  static constexpr int kTmemCols = 512;
+  __host__ __device__ static constexpr int s_col(int x, int buf) { return x * 256 + buf * BKV; }
+  __host__ __device__ static constexpr int o_col(int x) { return x * 256 + 2 * BKV; }
 };
 
 struct SwaParams {
   CUtensorMap tq, tk, tv;  // 4-D maps {d, dim1, dim2, batch}; boxes {64, ., ., 1}
   SwaArgs a;
   int seq_dim;             // 1 or 2: which map dimension is the sequence
+  int num_items, q_blocks;
 };
 
-// Coordinates of (column block x, head h, row t, batch b) in a 4-D map whose
-// dims 1 and 2 are (head, seq) or (seq, head).
 __device__ __forceinline__ void tma_rows(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
                                          int h, int t, int b, int seq_dim) {
   if (seq_dim == 2)
     tma_load_4d(dst, map, bar, x, h, t, b);
   else
     tma_load_4d(dst, map, bar, x, t, h, b);
+}
+
+__device__ __forceinline__ void prefetch_rows(const CUtensorMap* map, int x, int h, int t, int b,
+                                              int seq_dim) {
+  if (seq_dim == 2)
+    tma_prefetch_4d(map, x, h, t, b);
+  else
+    tma_prefetch_4d(map, x, t, h, b);
+}
+
+struct Item {
+  int q0, h, b, kt_hi, n_tiles;
+};
+
+// Items are ordered by query block, last (most key tiles) first, so the
+// round-robin split over CTAs hands out the long items before the short ones.
+__device__ __forceinline__ Item decode_item(const SwaParams& P, int item) {
+  Item it;
+  const int per_block = P.a.heads * P.a.batch;
+  const int qb = P.q_blocks - 1 - item / per_block;
+  const int rest = item % per_block;
+  it.h = rest % P.a.heads;
+  it.b = rest / P.a.heads;
+  it.q0 = qb * (QT * BQ);
+  const int k_first = max(0, it.q0 - P.a.window + 1);
+  const int k_last = min(P.a.seq - 1, it.q0 + QT * BQ - 1);
+  it.kt_hi = k_last / BKV;
+  it.n_tiles = it.kt_hi - k_first / BKV + 1;
+  return it;
+}
+
+// Does key tile [key0, key0 + 63] meet the band of query tile x of the item?
+__device__ __forceinline__ bool tile_relevant(const SwaParams& P, const Item& it, int x,
+                                              int key0) {
+  const int r0 = it.q0 + x * BQ;
+  if (r0 >= P.a.seq) return false;
+  const int r1 = min(r0 + BQ - 1, P.a.seq - 1);
+  return key0 <= r1 && key0 + BKV - 1 >= r0 - P.a.window + 1;
 }
 
 template <int D, bool COUNTS>
@@ -71,47 +120,39 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = sQ + C::kQBytes;                 // [NS][kKVBytes]
-  uint8_t* sV = sK + NS * C::kKVBytes;           // [NS][kKVBytes]
-  uint8_t* sP = sV + NS * C::kKVBytes;           // [2][kPBytes]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * C::kPBytes);
+  uint8_t* sQ = smem;                               // [QT][kQTileBytes]
+  uint8_t* sK = sQ + QT * C::kQTileBytes;           // [NS][kKVBytes]
+  uint8_t* sV = sK + NS * C::kKVBytes;              // [NS][kKVBytes]
+  uint8_t* sP = sV + NS * C::kKVBytes;              // [QT][2][kPBytes]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + QT * 2 * C::kPBytes);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = q_full + 1;       // [NS]
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* kv_full = q_empty + 1;      // [NS]
   uint64_t* kv_empty = kv_full + NS;    // [NS]
-  uint64_t* s_full = kv_empty + NS;     // [2]
-  uint64_t* p_full = s_full + 2;        // [2]
-  uint64_t* pv_full = p_full + 2;       // [2]
-  uint64_t* pv_empty = pv_full + 2;     // [2]
-  uint64_t* done_bar = pv_empty + 2;
+  uint64_t* s_full = kv_empty + NS;     // [QT][2]
+  uint64_t* p_full = s_full + 2 * QT;   // [QT][2]
+  uint64_t* pv_done = p_full + 2 * QT;  // [QT][2]
+  uint64_t* done_bar = pv_done + 2 * QT;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int q0 = blockIdx.x * BQ;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
-  const int seq = a.seq;
-  const int window = a.window;
-
-  // Key tiles intersecting the band of this query tile, walked downwards.
-  const int k_first = max(0, q0 - window + 1);
-  const int k_last = min(seq - 1, q0 + BQ - 1);
-  const int kt_hi = k_last / BKV;
-  const int n_tiles = kt_hi - k_first / BKV + 1;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);
-      mbar_init(&pv_full[i], 1);
-      mbar_init(&pv_empty[i], 4);
+    for (int x = 0; x < QT; ++x) {
+      mbar_init(&s_full[2 * x], 1);
+      mbar_init(&s_full[2 * x + 1], 1);
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(&p_full[2 * x + k], 4);
+        mbar_init(&pv_done[2 * x + k], 1);
+      }
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -135,81 +176,149 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
     // ------------------------------------------------------------- TMA --
     if (lane == 0) {
       bool ok = true;
+      uint32_t kv_count = 0, q_count = 0;
       uint32_t armed = 0, armed_parity = 0;
-      mbar_arrive_expect_tx(q_full, C::kQBytes);
-#pragma unroll
-      for (int at = 0; at < C::kAtoms; ++at)
-        tma_rows(sQ + at * BQ * 128, &P.tq, q_full, at * 64, h, q0, b, P.seq_dim);
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % NS;
-        const uint32_t ph = (j / NS) & 1;
-        if (!mbar_wait(&kv_empty[st], ph ^ 1u, abort_flag, a.status)) {
+      for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
+        const Item it = decode_item(P, item);
+        if (!mbar_wait(q_empty, (q_count & 1) ^ 1u, abort_flag, a.status)) {
           ok = false;
           break;
         }
-        const int key0 = (kt_hi - j) * BKV;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * C::kKVBytes);
+        const bool has_b = it.q0 + BQ < a.seq;
+        mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::kQTileBytes);
+        for (int x = 0; x < (has_b ? 2 : 1); ++x)
 #pragma unroll
-        for (int at = 0; at < C::kAtoms; ++at) {
-          tma_rows(sK + st * C::kKVBytes + at * BKV * 128, &P.tk, &kv_full[st], at * 64, h, key0,
-                   b, P.seq_dim);
-          tma_rows(sV + st * C::kKVBytes + at * BKV * 128, &P.tv, &kv_full[st], at * 64, h, key0,
-                   b, P.seq_dim);
+          for (int at = 0; at < C::kAtoms; ++at)
+            tma_rows(sQ + x * C::kQTileBytes + at * BQ * 128, &P.tq, q_full, at * 64, it.h,
+                     it.q0 + x * BQ, it.b, P.seq_dim);
+        ++q_count;
+        for (int j = 0; j < it.n_tiles; ++j, ++kv_count) {
+          const int st = kv_count % NS;
+          const uint32_t ph = (kv_count / NS) & 1;
+          if (!mbar_wait(&kv_empty[st], ph ^ 1u, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          const int key0 = (it.kt_hi - j) * BKV;
+          mbar_arrive_expect_tx(&kv_full[st], 2 * C::kKVBytes);
+#pragma unroll
+          for (int at = 0; at < C::kAtoms; ++at) {
+            tma_rows(sK + st * C::kKVBytes + at * BKV * 128, &P.tk, &kv_full[st], at * 64, it.h,
+                     key0, it.b, P.seq_dim);
+            tma_rows(sV + st * C::kKVBytes + at * BKV * 128, &P.tv, &kv_full[st], at * 64, it.h,
+                     key0, it.b, P.seq_dim);
+          }
+          armed |= 1u << st;
+          armed_parity = (armed_parity & ~(1u << st)) | (ph << st);
+          // Warm L2 with the tile kPrefetch positions ahead (into the next
+          // item, with its Q tiles, when this one runs out).
+          int pj = j + kPrefetch;
+          Item pit = it;
+          bool pvalid = true;
+          if (pj >= it.n_tiles) {
+            const int nxt = item + gridDim.x;
+            pvalid = nxt < P.num_items;
+            if (pvalid) {
+              pit = decode_item(P, nxt);
+              pj -= it.n_tiles;
+              pvalid = pj < pit.n_tiles;
+              if (pj == 0)
+                for (int x = 0; x < QT; ++x)
+                  if (pit.q0 + x * BQ < a.seq)
+#pragma unroll
+                    for (int at = 0; at < C::kAtoms; ++at)
+                      prefetch_rows(&P.tq, at * 64, pit.h, pit.q0 + x * BQ, pit.b, P.seq_dim);
+            }
+          }
+          if (pvalid) {
+            const int pkey0 = (pit.kt_hi - pj) * BKV;
+#pragma unroll
+            for (int at = 0; at < C::kAtoms; ++at) {
+              prefetch_rows(&P.tk, at * 64, pit.h, pkey0, pit.b, P.seq_dim);
+              prefetch_rows(&P.tv, at * 64, pit.h, pkey0, pit.b, P.seq_dim);
+            }
+          }
         }
-        armed |= 1u << st;
-        armed_parity = (armed_parity & ~(1u << st)) | (ph << st);
       }
+      // Let every copy this thread issued land before the CTA goes away.
       volatile int no_abort = 0;
-      if (!ok) {
-        for (int s = 0; s < NS; ++s)
-          if (armed & (1u << s))
-            mbar_wait(&kv_full[s], (armed_parity >> s) & 1u, &no_abort, a.status);
-      }
-      // The Q copy must have landed before the CTA can go away.
-      mbar_wait(q_full, 0, &no_abort, a.status);
+      for (int s = 0; s < NS; ++s)
+        if (armed & (1u << s))
+          mbar_wait(&kv_full[s], (armed_parity >> s) & 1u, &no_abort, a.status);
+      if (q_count > 0) mbar_wait(q_full, (q_count - 1) & 1, &no_abort, a.status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA --
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16(BQ, BKV);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(BQ, D) | (1u << 16);  // B (V) MN-major
-      bool ok = mbar_wait(q_full, 0, abort_flag, a.status);
-      tc_fence_after();
+      bool ok = true;
+      uint32_t kv_count = 0, q_count = 0;
+      uint32_t s_issued[QT] = {0, 0}, pv_issued[QT] = {0, 0};
       const uint32_t q_addr = smem_addr(sQ);
-      for (int j = 0; ok && j <= n_tiles; ++j) {
-        if (j < n_tiles) {
-          const int st = j % NS;
-          if (!mbar_wait(&kv_full[st], (j / NS) & 1, abort_flag, a.status)) break;
-          tc_fence_after();
-          const uint32_t k_addr = smem_addr(sK + st * C::kKVBytes);
-          const uint32_t d_tmem = tmem + C::kTmemS + (j & 1) * BKV;
+      for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
+        const Item it = decode_item(P, item);
+        if (!mbar_wait(q_full, q_count & 1, abort_flag, a.status)) break;
+        ++q_count;
+        tc_fence_after();
+        bool first_pv[QT] = {true, true};
+        for (int j = 0; ok && j <= it.n_tiles; ++j) {
+          if (j < it.n_tiles) {
+            const uint32_t kc = kv_count + j;
+            const int st = kc % NS;
+            if (!mbar_wait(&kv_full[st], (kc / NS) & 1, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int key0 = (it.kt_hi - j) * BKV;
+            const uint32_t k_addr = smem_addr(sK + st * C::kKVBytes);
+            for (int x = 0; x < QT; ++x) {
+              if (!tile_relevant(P, it, x, key0)) continue;
+              const int buf = s_issued[x] & 1;
+              const uint32_t d_tmem = tmem + C::s_col(x, buf);
+              const uint32_t qx = q_addr + x * C::kQTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t at = kk / 4, off = (kk % 4) * 32;
-            umma_bf16_ss(d_tmem, sw128_kmajor_desc(q_addr + at * BQ * 128 + off),
-                         sw128_kmajor_desc(k_addr + at * BKV * 128 + off), idesc_s, kk > 0);
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t at = kk / 4, off = (kk % 4) * 32;
+                umma_bf16_ss(d_tmem, sw128_kmajor_desc(qx + at * BQ * 128 + off),
+                             sw128_kmajor_desc(k_addr + at * BKV * 128 + off), idesc_s, kk > 0);
+              }
+              umma_commit(&s_full[2 * x + buf]);
+              ++s_issued[x];
+            }
+            if (j == it.n_tiles - 1) umma_commit(q_empty);  // Q is free once these finish
           }
-          umma_commit(&s_full[j & 1]);
-        }
-        if (j >= 1) {
-          const int t = j - 1;
-          const int pb = t & 1;
-          const uint32_t ph = (t >> 1) & 1;
-          if (!mbar_wait(&p_full[pb], ph, abort_flag, a.status) ||
-              !mbar_wait(&pv_empty[pb], ph ^ 1u, abort_flag, a.status))
-            break;
-          tc_fence_after();
-          const int st = t % NS;
-          const uint32_t p_addr = smem_addr(sP + pb * C::kPBytes);
-          const uint32_t v_addr = smem_addr(sV + st * C::kKVBytes);
-          const uint32_t d_tmem = tmem + C::kTmemPV + pb * D;
+          if (j >= 1) {
+            const int t = j - 1;
+            const uint32_t kc = kv_count + t;
+            const int st = kc % NS;
+            const int key0 = (it.kt_hi - t) * BKV;
+            const uint32_t v_addr = smem_addr(sV + st * C::kKVBytes);
+            for (int x = 0; x < QT; ++x) {
+              if (!tile_relevant(P, it, x, key0)) continue;
+              const uint32_t n = pv_issued[x];  // P V number n uses P buffer n % 2
+              if (!mbar_wait(&p_full[2 * x + (n & 1)], (n >> 1) & 1, abort_flag, a.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t p_addr = smem_addr(sP + (2 * x + (n & 1)) * C::kPBytes);
+              const uint32_t d_tmem = tmem + C::o_col(x);
 #pragma unroll
-          for (int kk = 0; kk < BKV / 16; ++kk)
-            umma_bf16_ss(d_tmem, sw128_kmajor_desc(p_addr + kk * 32),
-                         sw128_mnmajor_desc(v_addr + kk * 16 * 128, BKV * 128), idesc_pv, kk > 0);
-          umma_commit(&pv_full[pb]);
-          umma_commit(&kv_empty[st]);
+              for (int kk = 0; kk < BKV / 16; ++kk)
+                umma_bf16_ss(d_tmem, sw128_kmajor_desc(p_addr + kk * 32),
+                             sw128_mnmajor_desc(v_addr + kk * 16 * 128, BKV * 128), idesc_pv,
+                             (!first_pv[x] || kk > 0) ? 1u : 0u);
+              umma_commit(&pv_done[2 * x + (n & 1)]);
+              ++pv_issued[x];
+              first_pv[x] = false;
+            }
+            if (!ok) break;
+            umma_commit(&kv_empty[st]);
+          }
         }
+        kv_count += it.n_tiles;
       }
       umma_commit(done_bar);
       volatile int no_abort = 0;
@@ -217,122 +326,170 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
     }
   } else {
     // --------------------------------------------------------- softmax --
+    const int x = (warp - 2) >> 2;      // query tile of this warpgroup
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // row in the tile = TMEM lane
-    const int i = q0 + r;               // query position
+    const int r = quarter * 32 + lane;  // row in the query tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    float o[D];
-#pragma unroll
-    for (int c = 0; c < D; ++c) o[c] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
-    float alpha_ring[2] = {0.f, 0.f};
-    int cnt = 0;
+    const uint32_t o_tmem = tmem + lane_base + C::o_col(x);
+    uint32_t seen = 0;  // relevant tiles of this query tile so far (all items)
     bool ok = true;
 
-    auto fold_pv = [&](int t) -> bool {
-      const int pb = t & 1;
-      if (!mbar_wait(&pv_full[pb], (t >> 1) & 1, abort_flag, a.status)) return false;
+    // P V number n of this query tile is signalled on pv_done[x][n % 2];
+    // waits never lag a barrier by two phases (P V n + 2 needs P n + 2,
+    // which is only written after this wait).
+    auto wait_pv = [&](uint32_t n) -> bool {
+      if (!mbar_wait_warp(&pv_done[2 * x + (n & 1)], (n >> 1) & 1, abort_flag, a.status))
+        return false;
       tc_fence_after();
-      const float al = alpha_ring[pb];
-      const uint32_t base = tmem + lane_base + C::kTmemPV + pb * D;
-      if constexpr (D % 32 == 0) {
-#pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(base + c, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[c + e] = o[c + e] * al + __uint_as_float(v[e]);
-        }
-      } else {
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(base, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) o[e] = o[e] * al + __uint_as_float(v[e]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&pv_empty[pb]);
       return true;
     };
 
-    for (int j = 0; j < n_tiles; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, a.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float x[BKV];
-#pragma unroll
-      for (int c = 0; c < BKV; c += 32) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + C::kTmemS + sb * BKV + c, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[c + e] = __uint_as_float(v[e]) * a.scale_log2;
-      }
-      const int key0 = (kt_hi - j) * BKV;
-      const bool interior = (key0 + BKV - 1 <= i) && (key0 >= i - window + 1);
-      if (!interior) {
-#pragma unroll
-        for (int e = 0; e < BKV; ++e) {
-          const int kj = key0 + e;
-          const bool keep = (kj <= i) && (kj > i - window);
-          x[e] = keep ? x[e] : -INFINITY;
-          if (COUNTS) cnt += keep ? 1 : 0;
+    for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
+      const Item it = decode_item(P, item);
+      const int i = it.q0 + x * BQ + r;  // query position of this thread
+      if (it.q0 + x * BQ >= a.seq) continue;
+      float m_ref = -INFINITY, l_run = 0.f;
+      int cnt = 0;
+      bool any_pv = false;
+      for (int j = 0; j < it.n_tiles; ++j) {
+        const int key0 = (it.kt_hi - j) * BKV;
+        if (!tile_relevant(P, it, x, key0)) continue;
+        const int buf = seen & 1;
+        if (!mbar_wait_warp(&s_full[2 * x + buf], (seen >> 1) & 1, abort_flag, a.status)) {
+          ok = false;
+          break;
         }
-      } else if (COUNTS) {
-        cnt += BKV;
+        tc_fence_after();
+        float v[BKV];
+#pragma unroll
+        for (int c = 0; c < BKV; c += 32) {
+          uint32_t raw[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + C::s_col(x, buf) + c, raw);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[c + e] = __uint_as_float(raw[e]) * a.scale_log2;
+        }
+        const bool interior = (key0 + BKV - 1 <= i) && (key0 >= i - a.window + 1);
+        if (!interior) {
+#pragma unroll
+          for (int e = 0; e < BKV; ++e) {
+            const int kj = key0 + e;
+            const bool keep = (kj <= i) && (kj > i - a.window);
+            v[e] = keep ? v[e] : -INFINITY;
+            if (COUNTS) cnt += keep ? 1 : 0;
+          }
+        } else if (COUNTS) {
+          cnt += BKV;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < BKV; ++e) mx = fmaxf(mx, v[e]);
+        // Raise the reference max only when the row max passes it by 2^8.
+        float alpha = 1.f;
+        const bool raise = mx > m_ref + kRescaleLog2;
+        if (raise) {
+          alpha = fast_exp2(m_ref - mx);  // 0 while m_ref is -inf
+          l_run *= alpha;
+          m_ref = mx;
+        }
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        float rs = 0.f;
+        uint32_t pk[BKV / 2];
+#pragma unroll
+        for (int e = 0; e < BKV; e += 2) {
+          const float p0 = fast_exp2(v[e] - m_use);
+          const float p1 = fast_exp2(v[e + 1] - m_use);
+          rs += p0 + p1;
+          pk[e / 2] = pack_bf16x2(p0, p1);
+        }
+        l_run += rs;
+        // P buffer `buf` was last read by P V number seen - 2.
+        if (seen >= 2 && !wait_pv(seen - 2)) {
+          ok = false;
+          break;
+        }
+        uint8_t* prow = sP + (2 * x + buf) * C::kPBytes + r * 128;
+        // Row r of P: 64 keys = one 128-byte swizzled row; 16-byte chunk c
+        // sits at chunk position c ^ (r % 8).
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        if (any_pv && __any_sync(0xffffffffu, raise)) {
+          // O must hold every earlier P V of this item before it is rescaled.
+          if (!wait_pv(seen - 1)) {
+            ok = false;
+            break;
+          }
+          if constexpr (D % 32 == 0) {
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+              uint32_t o[32];
+              tmem_ld_32x32b_x32(o_tmem + c, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st_32x32b_x32(o_tmem + c, o);
+            }
+          } else {
+            uint32_t o[16];
+            tmem_ld_32x32b_x16(o_tmem, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st_32x32b_x16(o_tmem, o);
+          }
+          tmem_st_wait();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[2 * x + buf]);
+        any_pv = true;
+        ++seen;
       }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < BKV; ++e) mx = fmaxf(mx, x[e]);
-      const float m_new = fmaxf(m_run, mx);
-      const float m_ref = m_new == -INFINITY ? 0.f : m_new;
-      alpha_ring[sb] = fast_exp2(m_run - m_ref);
-      m_run = m_new;
-      float rs = 0.f;
-      uint32_t pk[BKV / 2];
-#pragma unroll
-      for (int e = 0; e < BKV; e += 2) {
-        const float p0 = fast_exp2(x[e] - m_ref);
-        const float p1 = fast_exp2(x[e + 1] - m_ref);
-        rs += p0 + p1;
-        pk[e / 2] = pack_bf16x2(p0, p1);
-      }
-      l_run = l_run * alpha_ring[sb] + rs;
-      // Row r of P_j, 64 keys = one 128-byte swizzled row: 16-byte chunk c
-      // of the row sits at chunk position c ^ (r % 8).
-      uint8_t* prow = sP + sb * C::kPBytes + r * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[sb]);
-      if (j >= 1 && !fold_pv(j - 1)) {
+      if (!ok) break;
+      // The last P V of the item, then O / l.
+      if (!wait_pv(seen - 1)) {
         ok = false;
         break;
       }
-    }
-    if (ok && n_tiles > 0) ok = fold_pv(n_tiles - 1);
-
-    if (ok && i < seq) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      __nv_bfloat16* orow = a.o + b * a.o_sb + h * a.o_sh + static_cast<int64_t>(i) * a.o_ss;
+      __nv_bfloat16* orow =
+          a.o + it.b * a.o_sb + it.h * a.o_sh + static_cast<int64_t>(i < a.seq ? i : 0) * a.o_ss;
+      if constexpr (D % 32 == 0) {
 #pragma unroll
-      for (int c = 0; c < D; c += 8) {
-        *reinterpret_cast<uint4*>(orow + c) =
-            make_uint4(pack_bf16x2(o[c] * inv, o[c + 1] * inv),
-                       pack_bf16x2(o[c + 2] * inv, o[c + 3] * inv),
-                       pack_bf16x2(o[c + 4] * inv, o[c + 5] * inv),
-                       pack_bf16x2(o[c + 6] * inv, o[c + 7] * inv));
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(o_tmem + c, o);
+          tmem_ld_wait();
+          if (i < a.seq) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 8)
+              *reinterpret_cast<uint4*>(orow + c + e) = make_uint4(
+                  pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
+                  pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
+                  pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
+                  pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+          }
+        }
+      } else {
+        uint32_t o[16];
+        tmem_ld_32x32b_x16(o_tmem, o);
+        tmem_ld_wait();
+        if (i < a.seq) {
+#pragma unroll
+          for (int e = 0; e < 16; e += 8)
+            *reinterpret_cast<uint4*>(orow + e) = make_uint4(
+                pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
+                pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
+                pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
+                pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+        }
       }
-      if (COUNTS) a.counts[(static_cast<int64_t>(b) * a.heads + h) * seq + i] = cnt;
+      tc_fence_before();
+      if (COUNTS && i < a.seq)
+        a.counts[(static_cast<int64_t>(it.b) * a.heads + it.h) * a.seq + i] = cnt;
     }
   }
 
@@ -346,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
 }
 
 template <int D, bool COUNTS>
-cudaError_t launch_typed(const SwaParams& prm, cudaStream_t stream) {
+cudaError_t launch_typed(const SwaParams& prm, int grid, cudaStream_t stream) {
   using C = SwaCfg<D>;
   auto kern = swa_tc_kernel<D, COUNTS>;
   static int configured_device = -1;
@@ -358,19 +515,18 @@ cudaError_t launch_typed(const SwaParams& prm, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const dim3 grid((prm.a.seq + BQ - 1) / BQ, prm.a.heads, prm.a.batch);
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(prm);
   return cudaGetLastError();
 }
 
 template <bool COUNTS>
-cudaError_t dispatch(const SwaParams& prm, cudaStream_t stream) {
+cudaError_t dispatch(const SwaParams& prm, int grid, cudaStream_t stream) {
   switch (prm.a.head_dim) {
-    case 16: return launch_typed<16, COUNTS>(prm, stream);
-    case 32: return launch_typed<32, COUNTS>(prm, stream);
-    case 64: return launch_typed<64, COUNTS>(prm, stream);
-    case 96: return launch_typed<96, COUNTS>(prm, stream);
-    case 128: return launch_typed<128, COUNTS>(prm, stream);
+    case 16: return launch_typed<16, COUNTS>(prm, grid, stream);
+    case 32: return launch_typed<32, COUNTS>(prm, grid, stream);
+    case 64: return launch_typed<64, COUNTS>(prm, grid, stream);
+    case 96: return launch_typed<96, COUNTS>(prm, grid, stream);
+    case 128: return launch_typed<128, COUNTS>(prm, grid, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -397,7 +553,6 @@ bool swa_map(CUtensorMap* map, const __nv_bfloat16* base, int64_t sb, int64_t sh
 
 cudaError_t launch_swa(const SwaArgs& a, cudaStream_t stream) {
   if (a.seq <= 0 || a.batch <= 0 || a.heads <= 0) return cudaSuccess;
-  if (a.batch > 65535 || a.heads > 65535) return cudaErrorInvalidValue;
   SwaParams prm;
   prm.a = a;
   int sd_q = 0, sd_k = 0, sd_v = 0;
@@ -413,7 +568,12 @@ cudaError_t launch_swa(const SwaArgs& a, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   if (sd_q != sd_k || sd_q != sd_v) return cudaErrorInvalidValue;
   prm.seq_dim = sd_q;
-  return a.counts ? dispatch<true>(prm, stream) : dispatch<false>(prm, stream);
+  prm.q_blocks = (a.seq + QT * BQ - 1) / (QT * BQ);
+  const int64_t items = static_cast<int64_t>(prm.q_blocks) * a.heads * a.batch;
+  if (items > 0x7fffffff) return cudaErrorInvalidValue;
+  prm.num_items = static_cast<int>(items);
+  const int grid = static_cast<int>(items < a.sms ? items : a.sms);
+  return a.counts ? dispatch<true>(prm, grid, stream) : dispatch<false>(prm, grid, stream);
 }
 
 }  // namespace ptb
