@@ -311,15 +311,28 @@ def run_ours(args, world, rank, local):
         return run_swa(args, world, rank, local)
     cfg = workload_config(args.workload)
     d = workloads.ptb_inputs(cfg, device="cuda")
-    ws = torch.empty(bsw.workspace_size(cfg.batch, cfg.seq, cfg.hidden, cfg.ffn),
-                     dtype=torch.uint8, device="cuda")
+    serial = args.block == "serial"
+    if serial:
+        ws = torch.empty(bsw.serial_workspace_size(cfg.batch, cfg.seq, cfg.hidden, cfg.ffn),
+                         dtype=torch.uint8, device="cuda")
+    else:
+        ws = torch.empty(bsw.workspace_size(cfg.batch, cfg.seq, cfg.hidden, cfg.ffn),
+                         dtype=torch.uint8, device="cuda")
     y = torch.empty_like(d["x"])
     fwd_args = (d["x"], d["ln_gamma"], d["ln_beta"], d["w_qkv"], d["w_o"], d["w_up"],
                 d["w_down"], cfg.heads, cfg.window)
     stream = torch.cuda.current_stream()
 
+    def layer(x_in, marks=None):
+        if serial:  # second LayerNorm: gamma = 1, beta = 0 like the first
+            return bsw.serial_forward(x_in, d["ln_gamma"], d["ln_beta"], d["ln_gamma"],
+                                      d["ln_beta"], *fwd_args[3:], y=y, workspace=ws)
+        if marks is not None:
+            return bsw.ptb_forward_events(x_in, *fwd_args[1:], marks, y=y, workspace=ws)
+        return bsw.ptb_forward(x_in, *fwd_args[1:], y=y, workspace=ws)
+
     for _ in range(args.warmup):
-        bsw.ptb_forward(*fwd_args, y=y, workspace=ws)
+        layer(d["x"])
     torch.cuda.synchronize()
     if bsw.last_device_error() != 0:
         raise RuntimeError("device status set during warm-up")
@@ -333,7 +346,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
-        bsw.ptb_forward_events(*fwd_args, marks[i], y=y, workspace=ws)
+        layer(d["x"], None if serial else marks[i])
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -343,18 +356,18 @@ def run_ours(args, world, rank, local):
     ms_local = t_start.elapsed_time(t_end) / args.steps
     ms = max_over_ranks(ms_local, world)
     names = ["layernorm", "gemm_qkv_up", "swa", "gemm_out_down"]
-    per_kernel = {n: sum(m[j].elapsed_time(m[j + 1]) for m in marks) / args.steps
-                  for j, n in enumerate(names)}
+    per_kernel = None if serial else {
+        n: sum(m[j].elapsed_time(m[j + 1]) for m in marks) / args.steps
+        for j, n in enumerate(names)}
 
     # End to end through the public call with host buffers: H2D of x, the
     # layer, D2H of y, every step.
     x_host = d["x"].cpu().pin_memory()
     y_host = torch.empty(d["x"].shape, dtype=torch.bfloat16, pin_memory=True)
     x_dev = torch.empty_like(d["x"])
-    e2e_args = (x_dev,) + fwd_args[1:]
     for _ in range(max(1, args.warmup)):
         x_dev.copy_(x_host, non_blocking=True)
-        bsw.ptb_forward(*e2e_args, y=y, workspace=ws)
+        layer(x_dev)
         y_host.copy_(y, non_blocking=True)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -364,7 +377,7 @@ def run_ours(args, world, rank, local):
     e0.record(stream)
     for _ in range(args.steps):
         x_dev.copy_(x_host, non_blocking=True)
-        bsw.ptb_forward(*e2e_args, y=y, workspace=ws)
+        layer(x_dev)
         y_host.copy_(y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -377,9 +390,15 @@ def run_ours(args, world, rank, local):
     tokens = cfg.tokens * world
     value = tokens / (ms * 1e-3)
     tflops = fl["total"] * world / (ms * 1e-3) / 1e12
-    g1_ms = per_kernel["gemm_qkv_up"]
-    g1_tf = fl["gemm1"] / (g1_ms * 1e-3) / 1e12
     peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    roofline = None
+    if per_kernel:
+        g1_tf = fl["gemm1"] / (per_kernel["gemm_qkv_up"] * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "gemm_qkv_up (tcgen05 [QKV|up] GEMM + GELU)",
+                    "achieved": g1_tf, "peak": peak_sus, "unit": "TFLOP/s",
+                    "frac": g1_tf / peak_sus, "peak_source": f"{peak_src} bf16 sustained",
+                    "traffic": traffic_for("gemm_qkv_up", args.workload, GEMM_SRC),
+                    "algorithmic_flops_per_launch": fl["gemm1"]}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -389,17 +408,15 @@ def run_ours(args, world, rank, local):
         "pct_of_peak": {"burst": 100 * tflops / world / peaks["bf16_tflops"],
                         "sustained": 100 * tflops / world / peak_sus, "source": peak_src},
         "kernels_ms": per_kernel,
-        "roofline": {"bound": "tensor", "kernel": "gemm_qkv_up (tcgen05 [QKV|up] GEMM + GELU)",
-                     "achieved": g1_tf, "peak": peak_sus, "unit": "TFLOP/s",
-                     "frac": g1_tf / peak_sus, "peak_source": f"{peak_src} bf16 sustained",
-                     "traffic": traffic_for("gemm_qkv_up", args.workload, GEMM_SRC),
-                     "algorithmic_flops_per_launch": fl["gemm1"]},
+        "roofline": roofline,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2},
         "clocks": clk,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (7 if serial else 4) * args.steps,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if serial:
+        line["block"] = "serial (h = x + Attn(LN1(x)), y = h + MLP(LN2(h)))"
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not serial:
         f64 = oracle_sample(cfg, args.cpu_rows, seed_device="cuda")
         times = time_oracle(cfg, f64, args.cpu_rows, 1)
         cpu_v = args.cpu_rows / times[0]
@@ -417,6 +434,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["175b", "13b", "530b", "tiny", "swa"], default="175b")
+    ap.add_argument("--block", choices=["ptb", "serial"], default="ptb",
+                    help="the parallel block (default) or the serial block it replaces")
     ap.add_argument("--cpu-rows", type=int, default=1024,
                     help="rows of the layer the CPU baseline computes (about 10 s of oracle work)")
     ap.add_argument("--ref-rows", type=int, default=64,

@@ -20,7 +20,7 @@ __all__ = [
     "PTBError", "load", "ptb_forward", "ptb_forward_events", "swa_attention",
     "swa_attention_strided", "swa_attention_counts", "layernorm", "gemm_qkv_up",
     "gemm_out_down", "gemm_workspace_size", "workspace_size", "release_workspace", "last_device_error",
-    "wait_probe", "LIB_PATH", "SYMBOLS",
+    "wait_probe", "serial_forward", "serial_workspace_size", "LIB_PATH", "SYMBOLS",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libptb.so")
@@ -39,6 +39,8 @@ SYMBOLS = {
     "ptb_forward": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p]),
     "ptb_forward_events": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p, _p, _i32]),
     "ptb_release_workspace": (_st, []),
+    "ptb_serial_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
+    "ptb_serial_forward": (_st, [_p] * 9 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p]),
     "ptb_forward_noalloc": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p]),
     "swa_attention": (_st, [_p, _p, _p, _i64, _i32, _i64, _i32, _i32, _f32, _p, _p]),
     "swa_attention_strided": (_st, [_p, _i64, _i64, _i64] * 4 + [_i64, _i32, _i64, _i32, _i32, _f32, _p]),
@@ -163,6 +165,26 @@ def ptb_forward_events(x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, heads: in
                                 _ptr(w_up), _ptr(w_down), batch, seq, hidden, ffn, heads, window,
                                 _ptr(y), _ptr(workspace), ws_bytes, _stream(stream), handles, 5)
     _check(st, "ptb_forward_events")
+    return y
+
+
+def serial_workspace_size(batch: int, seq: int, hidden: int, ffn: int) -> int:
+    return int(load().ptb_serial_workspace_size(batch, seq, hidden, ffn))
+
+
+def serial_forward(x, ln1_gamma, ln1_beta, ln2_gamma, ln2_beta, w_qkv, w_o, w_up, w_down,
+                   heads: int, window: int, y=None, workspace=None, stream=None):
+    """The serial block h = x + Attn(LN1(x)), y = h + MLP(LN2(h)); returns y."""
+    lib = load()
+    (batch, seq, hidden, ffn), y, ws_bytes = _ptb_args(
+        x, ln1_gamma, ln1_beta, w_qkv, w_o, w_up, w_down, heads, window, y, workspace)
+    for n, t in (("ln2_gamma", ln2_gamma), ("ln2_beta", ln2_beta)):
+        _bf16_cuda(n, t)
+    st = lib.ptb_serial_forward(_ptr(x), _ptr(ln1_gamma), _ptr(ln1_beta), _ptr(ln2_gamma),
+                                _ptr(ln2_beta), _ptr(w_qkv), _ptr(w_o), _ptr(w_up), _ptr(w_down),
+                                batch, seq, hidden, ffn, heads, window, _ptr(y), _ptr(workspace),
+                                ws_bytes, _stream(stream))
+    _check(st, "ptb_serial_forward")
     return y
 
 

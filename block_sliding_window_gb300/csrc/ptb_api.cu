@@ -99,32 +99,8 @@ int current_sms() {
   return 256;
 }
 
-// Split plans of the two GEMMs of one layer.
-struct LayerPlans {
-  GemmPlan g1, g2;
-  int bn1, bn2;
-};
-
-LayerPlans plan_layer(int64_t tokens, int64_t hidden, int64_t ffn, int sms) {
-  LayerPlans lp;
-  lp.bn1 = pick_block_n(3 * hidden, ffn);
-  lp.bn2 = pick_block_n(hidden, hidden);
-  const int64_t m_tiles = (tokens + 127) / 128;
-  lp.g1 = plan_gemm(m_tiles * ((3 * hidden + ffn) / (lp.bn1 ? lp.bn1 : 64)), hidden / 64, sms,
-                    lp.bn1 ? lp.bn1 : 64);
-  lp.g2 = plan_gemm(m_tiles * (hidden / (lp.bn2 ? lp.bn2 : 64)), (hidden + ffn) / 64, sms,
-                    lp.bn2 ? lp.bn2 : 64);
-  return lp;
-}
-
 size_t gemm_scratch_bytes(const GemmPlan& g) {
   return round_up(g.partial_bytes, kAlign) + round_up(g.counter_bytes, kAlign);
-}
-
-size_t layer_gemm_scratch(int64_t tokens, int64_t hidden, int64_t ffn, int sms) {
-  const LayerPlans lp = plan_layer(tokens, hidden, ffn, sms);
-  const size_t a = gemm_scratch_bytes(lp.g1), b = gemm_scratch_bytes(lp.g2);
-  return a > b ? a : b;
 }
 
 // Fills the grid / split fields of a launch.  Without scratch (or with too
@@ -153,62 +129,116 @@ __nv_bfloat16* bf(ptb_bf16* p) { return reinterpret_cast<__nv_bfloat16*>(p); }
 
 bool head_dim_ok(int64_t d) { return d == 16 || d == 32 || d == 64 || d == 96 || d == 128; }
 
+// One GEMM of the layer: C[M, N] = A[M, K] B[N, K]^T with
+//   A = [a0 | a1] split along K at k0 (k1 == 0: a0 only), and
+//   B = [b0 ; b1] split along N at n0 (n1 == 0: b0 only)
+// -- at most one split at a time.  In a K split b0 is [N, k0] and b1 is
+// [N, k1]; in an N split a0 is [M, K] and b0, b1 are [n0, K], [n1, K].
+struct GemmSpec {
+  const ptb_bf16 *a0, *a1, *b0, *b1;
+  int64_t lda0, lda1, k0, k1, n0, n1;
+  int64_t n() const { return n0 + n1; }
+  int64_t k() const { return k0 + k1; }
+  int block_n() const { return n1 ? pick_block_n(n0, n1) : pick_block_n(n0, n0); }
+};
+
+GemmSpec spec_plain(const ptb_bf16* a, int64_t lda, int64_t k, const ptb_bf16* b, int64_t n) {
+  return GemmSpec{a, a, b, b, lda, lda, k, 0, n, 0};
+}
+
+GemmPlan spec_plan(const GemmSpec& g, int64_t tokens, int sms) {
+  const int bn = g.block_n() ? g.block_n() : 64;
+  return plan_gemm((tokens + 127) / 128 * (g.n() / bn), g.k() / 64, sms, bn);
+}
+
+ptb_status gemm_run(DeviceState* ds, const GemmSpec& g, int64_t tokens, ptb_bf16* out, int64_t ldo,
+                    const ptb_bf16* resid, int64_t ldr, int64_t gelu_col, void* scratch,
+                    size_t scratch_bytes, cudaStream_t stream) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.block_n = g.block_n();
+  if (!a.block_n) return PTB_ERR_SHAPE;
+  const int64_t K = g.k(), N = g.n();
+  bool ok;
+  if (g.k1) {
+    ok = make_map(&a.a0, g.a0, g.k0, tokens, g.lda0, 128) &&
+         make_map(&a.a1, g.a1, g.k1, tokens, g.lda1, 128) &&
+         make_map(&a.b0, g.b0, g.k0, N, g.k0, a.block_n) &&
+         make_map(&a.b1, g.b1, g.k1, N, g.k1, a.block_n);
+  } else {
+    ok = make_map(&a.a0, g.a0, K, tokens, g.lda0, 128) &&
+         make_map(&a.a1, g.a0, K, tokens, g.lda0, 128) &&
+         make_map(&a.b0, g.b0, K, g.n0, K, a.block_n) &&
+         make_map(&a.b1, g.n1 ? g.b1 : g.b0, K, g.n1 ? g.n1 : g.n0, K, a.block_n);
+  }
+  if (!ok) return PTB_ERR_ARG;
+  a.M = static_cast<int>(tokens);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.n_split = static_cast<int>(g.n1 ? g.n0 : N);
+  a.k_split = static_cast<int>(g.k1 ? g.k0 : K);
+  a.out = bf(out);
+  a.ld_out = ldo;
+  a.resid = resid ? bf(resid) : nullptr;
+  a.ld_resid = ldr;
+  a.gelu_col = static_cast<int>(gelu_col);
+  a.epilogue = resid ? kEpiResidual : kEpiQkvGelu;
+  const int64_t tiles = (tokens + 127) / 128 * (N / a.block_n);
+  apply_plan(a, tiles, K / 64, ds->sms, scratch, scratch_bytes);
+  a.status = ds->status;
+  return launch_status(launch_gemm(a, stream));
+}
+
+// [QKV | up] of the PTB: U = [xn W_qkv^T | gelu(xn W_up^T)].
+GemmSpec spec_qkv_up(const ptb_bf16* xn, const ptb_bf16* w_qkv, const ptb_bf16* w_up,
+                     int64_t hidden, int64_t ffn) {
+  return GemmSpec{xn, xn, w_qkv, w_up, hidden, hidden, hidden, 0, 3 * hidden, ffn};
+}
+
+// [out | down] of the PTB: [ctx | G] [W_o | W_down]^T.
+GemmSpec spec_out_down(const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16* g, int64_t ld_g,
+                       const ptb_bf16* w_o, const ptb_bf16* w_down, int64_t hidden,
+                       int64_t ffn) {
+  return GemmSpec{ctx, g, w_o, w_down, ld_ctx, ld_g, hidden, ffn, hidden, 0};
+}
+
 ptb_status gemm_qkv_up(DeviceState* ds, const ptb_bf16* xn, const ptb_bf16* w_qkv,
                        const ptb_bf16* w_up, int64_t tokens, int64_t hidden, int64_t ffn,
                        ptb_bf16* u, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
-  GemmArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.block_n = pick_block_n(3 * hidden, ffn);
-  if (!a.block_n) return PTB_ERR_SHAPE;
-  const int64_t n = 3 * hidden + ffn;
-  if (!make_map(&a.a0, xn, hidden, tokens, hidden, 128) ||
-      !make_map(&a.a1, xn, hidden, tokens, hidden, 128) ||
-      !make_map(&a.b0, w_qkv, hidden, 3 * hidden, hidden, a.block_n) ||
-      !make_map(&a.b1, w_up, hidden, ffn, hidden, a.block_n))
-    return PTB_ERR_ARG;
-  a.M = static_cast<int>(tokens);
-  a.N = static_cast<int>(n);
-  a.K = static_cast<int>(hidden);
-  a.n_split = static_cast<int>(3 * hidden);
-  a.k_split = a.K;
-  a.out = bf(u);
-  a.ld_out = n;
-  a.gelu_col = static_cast<int>(3 * hidden);
-  a.epilogue = kEpiQkvGelu;
-  const int64_t tiles = (tokens + 127) / 128 * (n / a.block_n);
-  apply_plan(a, tiles, hidden / 64, ds->sms, scratch, scratch_bytes);
-  a.status = ds->status;
-  return launch_status(launch_gemm(a, stream));
+  return gemm_run(ds, spec_qkv_up(xn, w_qkv, w_up, hidden, ffn), tokens, u, 3 * hidden + ffn,
+                  nullptr, 0, 3 * hidden, scratch, scratch_bytes, stream);
 }
 
 ptb_status gemm_out_down(DeviceState* ds, const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16* g,
                          int64_t ld_g, const ptb_bf16* w_o, const ptb_bf16* w_down,
                          const ptb_bf16* x, int64_t tokens, int64_t hidden, int64_t ffn,
                          ptb_bf16* y, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
-  GemmArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.block_n = pick_block_n(hidden, hidden);
-  if (!a.block_n) return PTB_ERR_SHAPE;
-  if (!make_map(&a.a0, ctx, hidden, tokens, ld_ctx, 128) ||
-      !make_map(&a.a1, g, ffn, tokens, ld_g, 128) ||
-      !make_map(&a.b0, w_o, hidden, hidden, hidden, a.block_n) ||
-      !make_map(&a.b1, w_down, ffn, hidden, ffn, a.block_n))
-    return PTB_ERR_ARG;
-  a.M = static_cast<int>(tokens);
-  a.N = static_cast<int>(hidden);
-  a.K = static_cast<int>(hidden + ffn);
-  a.n_split = a.N;
-  a.k_split = static_cast<int>(hidden);
-  a.out = bf(y);
-  a.ld_out = hidden;
-  a.resid = bf(x);
-  a.ld_resid = hidden;
-  a.gelu_col = a.N;
-  a.epilogue = kEpiResidual;
-  const int64_t tiles = (tokens + 127) / 128 * (hidden / a.block_n);
-  apply_plan(a, tiles, (hidden + ffn) / 64, ds->sms, scratch, scratch_bytes);
-  a.status = ds->status;
-  return launch_status(launch_gemm(a, stream));
+  return gemm_run(ds, spec_out_down(ctx, ld_ctx, g, ld_g, w_o, w_down, hidden, ffn), tokens, y,
+                  hidden, x, hidden, hidden, scratch, scratch_bytes, stream);
+}
+
+// Scratch for the split last waves of the PTB's two GEMMs (the larger one).
+size_t layer_gemm_scratch(int64_t tokens, int64_t hidden, int64_t ffn, int sms) {
+  const ptb_bf16* z = nullptr;
+  const size_t a = gemm_scratch_bytes(spec_plan(spec_qkv_up(z, z, z, hidden, ffn), tokens, sms));
+  const size_t b = gemm_scratch_bytes(
+      spec_plan(spec_out_down(z, hidden, z, ffn, z, z, hidden, ffn), tokens, sms));
+  return a > b ? a : b;
+}
+
+// Scratch for the split last waves of the serial block's four GEMMs.
+size_t serial_gemm_scratch(int64_t tokens, int64_t hidden, int64_t ffn, int sms) {
+  const ptb_bf16* z = nullptr;
+  const GemmSpec specs[4] = {spec_plain(z, hidden, hidden, z, 3 * hidden),
+                             spec_plain(z, hidden, hidden, z, hidden),
+                             spec_plain(z, hidden, hidden, z, ffn),
+                             spec_plain(z, ffn, ffn, z, hidden)};
+  size_t m = 0;
+  for (const GemmSpec& g : specs) {
+    const size_t b = gemm_scratch_bytes(spec_plan(g, tokens, sms));
+    m = b > m ? b : m;
+  }
+  return m;
 }
 
 ptb_status check_gemm_shape(int64_t tokens, int64_t hidden, int64_t ffn) {
@@ -317,6 +347,83 @@ size_t ptb_gemm_workspace_size(int64_t tokens, int64_t hidden, int64_t ffn) {
   return layer_gemm_scratch(tokens, hidden, ffn, current_sms());
 }
 
+}  // extern "C"
+
+namespace ptb {
+namespace {
+
+// Argument checks shared by the layer entry points (before any device use).
+ptb_status check_layer(const void* const* ptrs, int nptrs, int64_t batch, int64_t seq,
+                       int64_t hidden, int64_t ffn, int32_t heads, int32_t window) {
+  for (int i = 0; i < nptrs; ++i)
+    if (!ptrs[i]) return PTB_ERR_ARG;
+  if (batch < 1 || seq < 1 || heads < 1 || window < 1) return PTB_ERR_ARG;
+  ptb_status st = check_gemm_shape(batch * seq, hidden, ffn);
+  if (st != PTB_OK) return st;
+  if (hidden > 32768 || hidden % heads) return PTB_ERR_SHAPE;
+  if (!head_dim_ok(hidden / heads)) return PTB_ERR_SHAPE;
+  if (batch * static_cast<int64_t>(heads) > 65535) return PTB_ERR_SHAPE;
+  for (int i = 0; i < nptrs; ++i)
+    if (!aligned(ptrs[i], 16)) return PTB_ERR_ALIGN;
+  return PTB_OK;
+}
+
+// The caller's workspace if given (checked), else the library arena grown to `need`.
+ptb_status acquire_workspace(DeviceState* ds, size_t need, void* workspace, size_t bytes,
+                             void** out) {
+  if (workspace) {
+    if (bytes < need) return PTB_ERR_WORKSPACE;
+    if (!aligned(workspace, kAlign)) return PTB_ERR_ALIGN;
+    *out = workspace;
+    return PTB_OK;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (ds->arena_bytes < need) {
+    if (ds->arena) {
+      cudaDeviceSynchronize();
+      cudaFree(ds->arena);
+      ds->arena = nullptr;
+      ds->arena_bytes = 0;
+    }
+    if (cudaMalloc(&ds->arena, need) != cudaSuccess) {
+      ds->arena = nullptr;
+      return PTB_ERR_DEVICE;
+    }
+    ds->arena_bytes = need;
+  }
+  *out = ds->arena;
+  return PTB_OK;
+}
+
+// Attention over the Q, K, V column blocks of U ([T, ldu]), output over Q.
+SwaArgs swa_over_u(DeviceState* ds, ptb_bf16* u, int64_t ldu, int64_t batch, int64_t seq,
+                   int64_t hidden, int32_t heads, int32_t window) {
+  const int64_t d = hidden / heads;
+  SwaArgs sa;
+  std::memset(&sa, 0, sizeof(sa));
+  sa.q = bf(u);
+  sa.k = bf(u) + hidden;
+  sa.v = bf(u) + 2 * hidden;
+  sa.o = bf(u);
+  sa.q_sb = sa.k_sb = sa.v_sb = sa.o_sb = seq * ldu;
+  sa.q_sh = sa.k_sh = sa.v_sh = sa.o_sh = d;
+  sa.q_ss = sa.k_ss = sa.v_ss = sa.o_ss = ldu;
+  sa.batch = static_cast<int>(batch);
+  sa.heads = heads;
+  sa.seq = static_cast<int>(seq);
+  sa.head_dim = static_cast<int>(d);
+  sa.window = window;
+  sa.scale_log2 = (1.0f / std::sqrt(static_cast<float>(d))) * 1.4426950408889634f;
+  sa.status = ds->status;
+  sa.sms = ds->sms;
+  return sa;
+}
+
+}  // namespace
+}  // namespace ptb
+
+extern "C" {
+
 ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
                               const ptb_bf16* ln_beta, const ptb_bf16* w_qkv,
                               const ptb_bf16* w_o, const ptb_bf16* w_up, const ptb_bf16* w_down,
@@ -325,17 +432,9 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
                               size_t workspace_bytes, ptb_stream stream_, void* const* events,
                               int32_t n_events) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  if (!x || !ln_gamma || !ln_beta || !w_qkv || !w_o || !w_up || !w_down || !y) return PTB_ERR_ARG;
-  if (batch < 1 || seq < 1 || heads < 1 || window < 1) return PTB_ERR_ARG;
-  ptb_status st = check_gemm_shape(batch * seq, hidden, ffn);
-  if (st != PTB_OK) return st;
-  if (hidden > 32768 || hidden % heads) return PTB_ERR_SHAPE;
-  const int64_t d = hidden / heads;
-  if (!head_dim_ok(d)) return PTB_ERR_SHAPE;
-  if (batch * static_cast<int64_t>(heads) > 65535) return PTB_ERR_SHAPE;
   const void* ptrs[] = {x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, y};
-  for (const void* p : ptrs)
-    if (!aligned(p, 16)) return PTB_ERR_ALIGN;
+  ptb_status st = check_layer(ptrs, 8, batch, seq, hidden, ffn, heads, window);
+  if (st != PTB_OK) return st;
   if (events && n_events != 5) return PTB_ERR_ARG;
   if (events)
     for (int i = 0; i < 5; ++i)
@@ -346,26 +445,8 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
 
   const int64_t tokens = batch * seq;
   const size_t need = ptb_forward_workspace_size(batch, seq, hidden, ffn);
-  if (workspace) {
-    if (workspace_bytes < need) return PTB_ERR_WORKSPACE;
-    if (!aligned(workspace, kAlign)) return PTB_ERR_ALIGN;
-  } else {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (ds->arena_bytes < need) {
-      if (ds->arena) {
-        cudaDeviceSynchronize();
-        cudaFree(ds->arena);
-        ds->arena = nullptr;
-        ds->arena_bytes = 0;
-      }
-      if (cudaMalloc(&ds->arena, need) != cudaSuccess) {
-        ds->arena = nullptr;
-        return PTB_ERR_DEVICE;
-      }
-      ds->arena_bytes = need;
-    }
-    workspace = ds->arena;
-  }
+  st = acquire_workspace(ds, need, workspace, workspace_bytes, &workspace);
+  if (st != PTB_OK) return st;
   ptb_bf16* xn = static_cast<ptb_bf16*>(workspace);
   ptb_bf16* u = reinterpret_cast<ptb_bf16*>(static_cast<char*>(workspace) +
                                             round_up(tokens * hidden * 2, kAlign));
@@ -392,24 +473,8 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
   if (st != PTB_OK) return st;
   // 3. ctx = SWA(Q, K, V), written over Q inside U
   if (!mark(2)) return PTB_ERR_ARG;
-  SwaArgs sa;
-  std::memset(&sa, 0, sizeof(sa));
-  sa.q = bf(u);
-  sa.k = bf(u) + hidden;
-  sa.v = bf(u) + 2 * hidden;
-  sa.o = bf(u);
-  sa.q_sb = sa.k_sb = sa.v_sb = sa.o_sb = seq * ldu;
-  sa.q_sh = sa.k_sh = sa.v_sh = sa.o_sh = d;
-  sa.q_ss = sa.k_ss = sa.v_ss = sa.o_ss = ldu;
-  sa.batch = static_cast<int>(batch);
-  sa.heads = heads;
-  sa.seq = static_cast<int>(seq);
-  sa.head_dim = static_cast<int>(d);
-  sa.window = window;
-  sa.scale_log2 = (1.0f / std::sqrt(static_cast<float>(d))) * 1.4426950408889634f;
-  sa.status = ds->status;
-  sa.sms = ds->sms;
-  if (launch_swa(sa, stream) != cudaSuccess) return PTB_ERR_LAUNCH;
+  if (launch_swa(swa_over_u(ds, u, ldu, batch, seq, hidden, heads, window), stream) != cudaSuccess)
+    return PTB_ERR_LAUNCH;
   // 4. y = x + [ctx | G] [W_o | W_down]^T
   if (!mark(3)) return PTB_ERR_ARG;
   st = gemm_out_down(ds, u, ldu, u + 3 * hidden, ldu, w_o, w_down, x, tokens, hidden, ffn, y,
@@ -417,6 +482,67 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
   if (st != PTB_OK) return st;
   if (!mark(4)) return PTB_ERR_ARG;
   return PTB_OK;
+}
+
+size_t ptb_serial_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn) {
+  if (batch < 1 || seq < 1 || hidden < 1 || ffn < 1) return 0;
+  const size_t t = static_cast<size_t>(batch) * static_cast<size_t>(seq);
+  size_t gemm = 0;
+  if (hidden % 64 == 0 && ffn % 64 == 0)
+    gemm = serial_gemm_scratch(static_cast<int64_t>(t), hidden, ffn, current_sms());
+  return 2 * round_up(t * hidden * 2, kAlign) + round_up(t * (3 * hidden + ffn) * 2, kAlign) + gemm;
+}
+
+ptb_status ptb_serial_forward(const ptb_bf16* x, const ptb_bf16* ln1_gamma,
+                              const ptb_bf16* ln1_beta, const ptb_bf16* ln2_gamma,
+                              const ptb_bf16* ln2_beta, const ptb_bf16* w_qkv, const ptb_bf16* w_o,
+                              const ptb_bf16* w_up, const ptb_bf16* w_down, int64_t batch,
+                              int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
+                              int32_t window, ptb_bf16* y, void* workspace,
+                              size_t workspace_bytes, ptb_stream stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const void* ptrs[] = {x, ln1_gamma, ln1_beta, ln2_gamma, ln2_beta, w_qkv, w_o, w_up, w_down, y};
+  ptb_status st = check_layer(ptrs, 10, batch, seq, hidden, ffn, heads, window);
+  if (st != PTB_OK) return st;
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != PTB_OK) return st;
+
+  const int64_t tokens = batch * seq;
+  const size_t need = ptb_serial_workspace_size(batch, seq, hidden, ffn);
+  st = acquire_workspace(ds, need, workspace, workspace_bytes, &workspace);
+  if (st != PTB_OK) return st;
+  char* base = static_cast<char*>(workspace);
+  const size_t act = round_up(tokens * hidden * 2, kAlign);
+  ptb_bf16* xn = reinterpret_cast<ptb_bf16*>(base);
+  ptb_bf16* h = reinterpret_cast<ptb_bf16*>(base + act);
+  ptb_bf16* u = reinterpret_cast<ptb_bf16*>(base + 2 * act);
+  char* scratch = reinterpret_cast<char*>(u) + round_up(tokens * (3 * hidden + ffn) * 2, kAlign);
+  const size_t scratch_size = need - static_cast<size_t>(scratch - base);
+  const int64_t ldu = 3 * hidden + ffn;
+  const int hid = static_cast<int>(hidden);
+
+  // h = x + Attn(LN1(x))
+  if (launch_layernorm(bf(x), bf(ln1_gamma), bf(ln1_beta), tokens, hid, 1e-5f, bf(xn), stream) !=
+      cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  st = gemm_run(ds, spec_plain(xn, hidden, hidden, w_qkv, 3 * hidden), tokens, u, ldu, nullptr, 0,
+                3 * hidden, scratch, scratch_size, stream);
+  if (st != PTB_OK) return st;
+  if (launch_swa(swa_over_u(ds, u, ldu, batch, seq, hidden, heads, window), stream) != cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  st = gemm_run(ds, spec_plain(u, ldu, hidden, w_o, hidden), tokens, h, hidden, x, hidden, hidden,
+                scratch, scratch_size, stream);
+  if (st != PTB_OK) return st;
+  // y = h + MLP(LN2(h))
+  if (launch_layernorm(bf(h), bf(ln2_gamma), bf(ln2_beta), tokens, hid, 1e-5f, bf(xn), stream) !=
+      cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  st = gemm_run(ds, spec_plain(xn, hidden, hidden, w_up, ffn), tokens, u + 3 * hidden, ldu,
+                nullptr, 0, 0, scratch, scratch_size, stream);
+  if (st != PTB_OK) return st;
+  return gemm_run(ds, spec_plain(u + 3 * hidden, ldu, ffn, w_down, hidden), tokens, y, hidden, h,
+                  hidden, hidden, scratch, scratch_size, stream);
 }
 
 ptb_status ptb_forward(const ptb_bf16* x, const ptb_bf16* ln_gamma, const ptb_bf16* ln_beta,

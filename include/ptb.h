@@ -149,6 +149,26 @@ ptb_status ptb_forward_noalloc(const ptb_bf16* x, const ptb_bf16* ln_gamma,
                                int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,
                                int32_t heads, int32_t window, ptb_bf16* y, ptb_stream stream);
 
+/*
+ * ptb_serial_forward: the serial block that the PTB replaces (MegaScale
+ * notes, §2.2, PTB row, where it is printed without the attention residual;
+ * read here as the standard pre-LN block):
+ *   h = x + Attn(LN1(x)),   y = h + MLP(LN2(h)).
+ * Same weights, layouts, shape rules and errors as ptb_forward, plus a
+ * second LayerNorm (ln2_gamma, ln2_beta).  Seven kernels in order: LN1,
+ * QKV GEMM, SWA, out-projection GEMM + x, LN2, up-projection GEMM + GELU,
+ * down-projection GEMM + h.  workspace as for ptb_forward, sized by
+ * ptb_serial_workspace_size().
+ */
+size_t ptb_serial_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn);
+ptb_status ptb_serial_forward(const ptb_bf16* x, const ptb_bf16* ln1_gamma,
+                              const ptb_bf16* ln1_beta, const ptb_bf16* ln2_gamma,
+                              const ptb_bf16* ln2_beta, const ptb_bf16* w_qkv, const ptb_bf16* w_o,
+                              const ptb_bf16* w_up, const ptb_bf16* w_down, int64_t batch,
+                              int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
+                              int32_t window, ptb_bf16* y, void* workspace,
+                              size_t workspace_bytes, ptb_stream stream);
+
 /* Frees the library's own workspace arena on the current device (if any). */
 ptb_status ptb_release_workspace(void);
 

@@ -210,18 +210,22 @@ def ptb_forward(x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down,
 
 
 def serial_block(x, ln1_gamma, ln1_beta, ln2_gamma, ln2_beta, w_qkv, w_o,
-                 w_up, w_down, heads: int, window: int,
+                 w_up, w_down, heads: int, window: int, rows=None,
                  eps: float = LN_EPS) -> np.ndarray:
     """The serial block that PTB replaces: h = x + Attn(LN1(x)),
     y = h + MLP(LN2(h)).
 
     The notes print the serial form with the attention residual missing
     (MegaScale notes, §2.2, PTB row); this is the standard pre-LN reading.
-    Used only to check PTB's special cases against it."""
+    rows: optional sequence positions, as in ptb_forward (the MLP half is
+    row-local, so only the attention half needs the window's keys)."""
     x = _f64(x)
-    pos = np.arange(x.shape[1])
-    u1 = layer_norm(x, ln1_gamma, ln1_beta, eps)
-    h = x + attention_branch(u1, u1, w_qkv, w_o, heads, window, pos, pos)
+    seq = x.shape[1]
+    q_pos = np.arange(seq) if rows is None else np.asarray(rows, dtype=np.int64)
+    k_pos = np.arange(seq) if rows is None else needed_key_positions(q_pos, window)
+    u1_q = layer_norm(x[:, q_pos], ln1_gamma, ln1_beta, eps)
+    u1_k = u1_q if rows is None else layer_norm(x[:, k_pos], ln1_gamma, ln1_beta, eps)
+    h = x[:, q_pos] + attention_branch(u1_q, u1_k, w_qkv, w_o, heads, window, q_pos, k_pos)
     u2 = layer_norm(h, ln2_gamma, ln2_beta, eps)
     return h + mlp_branch(u2, w_up, w_down)
 

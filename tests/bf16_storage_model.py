@@ -47,3 +47,29 @@ def ptb_forward_bf16_storage(x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, hea
         ctx[:, sl] = (bf16(e) @ v[:, sl]) / e.sum(axis=1, keepdims=True)
     ctx = bf16(ctx)
     return bf16(x0[rows] + oracle.linear(ctx, w_o) + oracle.linear(g, w_down))
+
+
+def serial_bf16_storage(x, g1, b1, g2, b2, w_qkv, w_o, w_up, w_down, heads, window, rows):
+    """The serial block with bf16 storage of xn1, Q, K, V, P, ctx, h, xn2,
+    G and y (batch entry 0, positions `rows`)."""
+    f = lambda t: t.detach().to("cpu").double().numpy() if hasattr(t, "detach") else np.asarray(t, np.float64)  # noqa: E731
+    x0 = f(x[0])
+    hidden = x0.shape[-1]
+    d = hidden // heads
+    kpos = oracle.needed_key_positions(rows, window)
+    need = np.union1d(kpos, rows)
+    xn = np.zeros_like(x0)
+    xn[need] = bf16(oracle.layer_norm(x0[need], g1, b1))
+    q = bf16(oracle.linear(xn[rows], w_qkv[0:hidden]))
+    k = bf16(oracle.linear(xn[kpos], w_qkv[hidden:2 * hidden]))
+    v = bf16(oracle.linear(xn[kpos], w_qkv[2 * hidden:3 * hidden]))
+    ctx = np.zeros((len(rows), hidden))
+    mask = oracle.band_mask(rows, kpos, window)
+    for hh in range(heads):
+        sl = slice(hh * d, (hh + 1) * d)
+        s = np.where(mask, (q[:, sl] @ k[:, sl].T) / math.sqrt(d), -np.inf)
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        ctx[:, sl] = (bf16(e) @ v[:, sl]) / e.sum(axis=1, keepdims=True)
+    h = bf16(x0[rows] + oracle.linear(bf16(ctx), w_o))
+    g = bf16(oracle.gelu_tanh(oracle.linear(bf16(oracle.layer_norm(h, g2, b2)), w_up)))
+    return bf16(h + oracle.linear(g, w_down))

@@ -81,3 +81,20 @@ def swa(q, k, v, window, scale=None):
                        for i in range(len(qh))])
         res.append(hs)
     return res
+
+
+def serial(x, g1, b1, g2, b2, w_qkv, w_o, w_up, w_down, heads, window, eps=1e-5):
+    """The serial pre-LN block h = x + Attn(LN1(x)), y = h + MLP(LN2(h)), by
+    looping: the attention half is the PTB with a zero MLP, the MLP half is
+    written out row by row."""
+    zeros_down = [[0.0] * len(w_down[0]) for _ in w_down]
+    h = ptb(x, g1, b1, w_qkv, w_o, w_up, zeros_down, heads, window, eps)
+    out = []
+    for seq in h:
+        rows = []
+        for row in seq:
+            u = _layer_norm_row(row, g2, b2, eps)
+            mlp = _matvec(w_down, [_gelu(a) for a in _matvec(w_up, u)])
+            rows.append([row[c] + mlp[c] for c in range(len(row))])
+        out.append(rows)
+    return out

@@ -16,7 +16,7 @@ import torch
 
 import oracle
 from block_sliding_window_gb300 import workloads
-from tests.bf16_storage_model import ptb_forward_bf16_storage
+from tests.bf16_storage_model import ptb_forward_bf16_storage, serial_bf16_storage
 from tests.parity import MAX_ABS, REL_L2, assert_close, errors, to_np
 
 pytestmark = pytest.mark.gpu
@@ -237,6 +237,49 @@ def test_ptb_special_case_attention_off(ptb_lib):
         want = oracle.ptb_forward(h2["x"], h2["ln_gamma"], h2["ln_beta"], h2["w_qkv"], h2["w_o"],
                                   h2["w_up"], h2["w_down"], cfg.heads, cfg.window)
         assert_close(y, want, f"{zero} = 0")
+
+
+def _ln2(hidden, seed):
+    g2 = workloads.normal_bf16((hidden,), seed=seed, std=0.1, mean=1.0)
+    b2 = workloads.normal_bf16((hidden,), seed=seed + 1, std=0.1)
+    return g2, b2
+
+
+@pytest.mark.parametrize("cfg", SMALL_LAYERS, ids=lambda c: c.name)
+def test_serial_forward_small(ptb_lib, cfg):
+    host = workloads.ptb_inputs(cfg)
+    g2, b2 = _ln2(cfg.hidden, 31)
+    d = _cuda(host)
+    y = ptb_lib.serial_forward(d["x"], d["ln_gamma"], d["ln_beta"], g2.cuda(), b2.cuda(),
+                               d["w_qkv"], d["w_o"], d["w_up"], d["w_down"], cfg.heads, cfg.window)
+    want = oracle.serial_block(host["x"], host["ln_gamma"], host["ln_beta"], g2, b2, host["w_qkv"],
+                               host["w_o"], host["w_up"], host["w_down"], cfg.heads, cfg.window)
+    assert_close(y, want, "serial " + cfg.name)
+
+
+@pytest.mark.parametrize("name", ["13b", "175b"])
+def test_serial_forward_full_size_sampled(ptb_lib, name):
+    cfg = workloads.PTB_CONFIGS[name]
+    d = workloads.ptb_inputs(cfg, device="cuda")
+    g2, b2 = _ln2(cfg.hidden, 33)
+    ws = torch.empty(ptb_lib.serial_workspace_size(cfg.batch, cfg.seq, cfg.hidden, cfg.ffn),
+                     dtype=torch.uint8, device="cuda")
+    y = ptb_lib.serial_forward(d["x"], d["ln_gamma"], d["ln_beta"], g2.cuda(), b2.cuda(),
+                               d["w_qkv"], d["w_o"], d["w_up"], d["w_down"], cfg.heads, cfg.window,
+                               workspace=ws)
+    torch.cuda.synchronize()
+    rows = workloads.sample_rows(cfg.seq, cfg.window)
+    host = {k: v.cpu() for k, v in d.items()}
+    del d, ws
+    args = (host["x"], host["ln_gamma"], host["ln_beta"], g2, b2, host["w_qkv"], host["w_o"],
+            host["w_up"], host["w_down"], cfg.heads, cfg.window)
+    want = oracle.serial_block(*args, rows=rows)
+    _, _, floor = errors(serial_bf16_storage(*args, rows), want[0])
+    rel, mx, ex = errors(y[0, rows], want[0])
+    bound = max(MAX_ABS, 1.25 * floor)
+    print(f"serial {name}: rel-L2 {rel:.3e}, max-abs {mx:.3e}, beyond rounding {ex:.3e}, "
+          f"bf16-storage floor {floor:.3e}, bound {bound:.3e}")
+    assert rel <= REL_L2 and ex <= bound
 
 
 @pytest.mark.parametrize("name", ["13b", "175b", "530b"])

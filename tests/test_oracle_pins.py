@@ -157,6 +157,19 @@ def check_brute_force_swa():
         assert np.allclose(oracle.swa(q, k, v, w), ref, rtol=1e-12, atol=1e-12), w
 
 
+def check_brute_force_serial():
+    b, s, h, nh, f, w = 2, 7, 8, 2, 12, 3
+    p = _rand_ptb(11, b, s, h, nh, f)
+    r = _rng(12)
+    g2, b2 = 1.0 + 0.1 * r.standard_normal(h), 0.1 * r.standard_normal(h)
+    got = oracle.serial_block(p["x"], p["ln_gamma"], p["ln_beta"], g2, b2, p["w_qkv"], p["w_o"],
+                              p["w_up"], p["w_down"], nh, w)
+    ref = brute_force.serial(p["x"].tolist(), p["ln_gamma"].tolist(), p["ln_beta"].tolist(),
+                             g2.tolist(), b2.tolist(), p["w_qkv"].tolist(), p["w_o"].tolist(),
+                             p["w_up"].tolist(), p["w_down"].tolist(), nh, w)
+    assert np.allclose(got, np.array(ref), rtol=1e-11, atol=1e-11)
+
+
 def check_ptb_special_cases():
     b, s, h, nh, f, w = 2, 12, 16, 4, 24, 5
     p = _rand_ptb(7, b, s, h, nh, f)
@@ -213,13 +226,20 @@ def check_row_sampling():
     part = oracle.ptb_forward(*args, rows=rows)
     assert np.allclose(part, full[:, rows], rtol=1e-13, atol=1e-13)
     assert list(oracle.needed_key_positions([0, 6, 39], w)) == [0, 1, 2, 3, 4, 5, 6, 34, 35, 36, 37, 38, 39]
+    g2, b2 = p["ln_gamma"][::-1].copy(), p["ln_beta"][::-1].copy()
+    sargs = (p["x"], p["ln_gamma"], p["ln_beta"], g2, b2, p["w_qkv"], p["w_o"], p["w_up"],
+             p["w_down"], nh, w)
+    sfull = oracle.serial_block(*sargs)
+    assert np.allclose(oracle.serial_block(*sargs, rows=rows), sfull[:, rows], rtol=1e-13,
+                       atol=1e-13)
 
 
 # ----------------------------------------------------------------- tests --
 
 CHECKS = [check_counts_closed_form, check_window1_is_v, check_full_causal_vs_sdpa,
           check_band_vs_sdpa, check_convex_rows, check_layer_norm, check_gelu,
-          check_brute_force_ptb, check_brute_force_swa, check_ptb_special_cases,
+          check_brute_force_ptb, check_brute_force_swa, check_brute_force_serial,
+          check_ptb_special_cases,
           check_head_permutation, check_row_sampling]
 
 
@@ -300,6 +320,7 @@ MUTATIONS = [
     ("layer_norm", _bad_ln_unbiased, check_layer_norm),
     ("gelu_tanh", _bad_gelu_sign, check_gelu),
     ("mlp_branch", _bad_mlp_dropped, check_brute_force_ptb),
+    ("mlp_branch", _bad_mlp_dropped, check_brute_force_serial),
     ("attention_branch", _bad_attn_transposed_wo, check_brute_force_ptb),
 ]
 
