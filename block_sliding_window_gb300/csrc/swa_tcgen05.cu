@@ -12,10 +12,9 @@
 //   warp 0      TMA: the two Q tiles of an item, then the 64-key K and V
 //               tiles intersecting the item's band [q0 - w + 1, q0 + 255]
 //               (diagonal tile first) into a 3-stage ring that runs on
-//               across items, with the tiles four positions ahead (and the
-//               next item's Q) prefetched into L2 so that ring loads do not
-//               pay DRAM latency.  d < 128 is read as 64-wide boxes;
-//               columns past d are zero-filled by TMA.
+//               across items.  d < 128 is read as 64-wide boxes; columns
+//               past d are zero-filled by TMA.  (An L2 prefetch of the tiles
+//               four positions ahead was measured slightly slower.)
 //   warp 1      owns TMEM (512 columns: per query tile two 64-column score
 //               buffers and a d-column output accumulator); one thread issues
 //                 S_X = Q_X K_j^T   (M 128, N 64, K d)
@@ -45,7 +44,6 @@ constexpr int BKV = 64;       // keys per K/V tile (= MMA N of S, K of PV)
 constexpr int NS = 3;         // K/V stages
 constexpr int kThreads = 320;
 constexpr float kRescaleLog2 = 8.0f;  // raise the reference max only past 2^8
-constexpr int kPrefetch = 4;          // K/V tiles prefetched into L2 ahead of the ring
 
 template <int D>
 struct SwaCfg {
@@ -73,14 +71,6 @@ __device__ __forceinline__ void tma_rows(void* dst, const CUtensorMap* map, uint
     tma_load_4d(dst, map, bar, x, h, t, b);
   else
     tma_load_4d(dst, map, bar, x, t, h, b);
-}
-
-__device__ __forceinline__ void prefetch_rows(const CUtensorMap* map, int x, int h, int t, int b,
-                                              int seq_dim) {
-  if (seq_dim == 2)
-    tma_prefetch_4d(map, x, h, t, b);
-  else
-    tma_prefetch_4d(map, x, t, h, b);
 }
 
 struct Item {
@@ -210,34 +200,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
           }
           armed |= 1u << st;
           armed_parity = (armed_parity & ~(1u << st)) | (ph << st);
-          // Warm L2 with the tile kPrefetch positions ahead (into the next
-          // item, with its Q tiles, when this one runs out).
-          int pj = j + kPrefetch;
-          Item pit = it;
-          bool pvalid = true;
-          if (pj >= it.n_tiles) {
-            const int nxt = item + gridDim.x;
-            pvalid = nxt < P.num_items;
-            if (pvalid) {
-              pit = decode_item(P, nxt);
-              pj -= it.n_tiles;
-              pvalid = pj < pit.n_tiles;
-              if (pj == 0)
-                for (int x = 0; x < QT; ++x)
-                  if (pit.q0 + x * BQ < a.seq)
-#pragma unroll
-                    for (int at = 0; at < C::kAtoms; ++at)
-                      prefetch_rows(&P.tq, at * 64, pit.h, pit.q0 + x * BQ, pit.b, P.seq_dim);
-            }
-          }
-          if (pvalid) {
-            const int pkey0 = (pit.kt_hi - pj) * BKV;
-#pragma unroll
-            for (int at = 0; at < C::kAtoms; ++at) {
-              prefetch_rows(&P.tk, at * 64, pit.h, pkey0, pit.b, P.seq_dim);
-              prefetch_rows(&P.tv, at * 64, pit.h, pkey0, pit.b, P.seq_dim);
-            }
-          }
         }
       }
       // Let every copy this thread issued land before the CTA goes away.
