@@ -312,7 +312,13 @@ def run_ours(args, world, rank, local):
     cfg = workload_config(args.workload)
     d = workloads.ptb_inputs(cfg, device="cuda")
     serial = args.block == "serial"
-    if serial:
+    fp8 = args.precision == "fp8"
+    w8 = None
+    if fp8:  # weights quantized once, outside the timed region
+        w8 = bsw.prepare_fp8_weights(d["w_qkv"], d["w_o"], d["w_up"], d["w_down"])
+        ws = torch.empty(bsw.fp8_workspace_size(cfg.batch, cfg.seq, cfg.hidden, cfg.ffn),
+                         dtype=torch.uint8, device="cuda")
+    elif serial:
         ws = torch.empty(bsw.serial_workspace_size(cfg.batch, cfg.seq, cfg.hidden, cfg.ffn),
                          dtype=torch.uint8, device="cuda")
     else:
@@ -324,6 +330,9 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream()
 
     def layer(x_in, marks=None):
+        if fp8:
+            return bsw.ptb_forward_fp8(x_in, d["ln_gamma"], d["ln_beta"], w8, cfg.heads,
+                                       cfg.window, y=y, workspace=ws)
         if serial:  # second LayerNorm: gamma = 1, beta = 0 like the first
             return bsw.serial_forward(x_in, d["ln_gamma"], d["ln_beta"], d["ln_gamma"],
                                       d["ln_beta"], *fwd_args[3:], y=y, workspace=ws)
@@ -346,7 +355,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
-        layer(d["x"], None if serial else marks[i])
+        layer(d["x"], None if (serial or fp8) else marks[i])
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -356,7 +365,7 @@ def run_ours(args, world, rank, local):
     ms_local = t_start.elapsed_time(t_end) / args.steps
     ms = max_over_ranks(ms_local, world)
     names = ["layernorm", "gemm_qkv_up", "swa", "gemm_out_down"]
-    per_kernel = None if serial else {
+    per_kernel = None if (serial or fp8) else {
         n: sum(m[j].elapsed_time(m[j + 1]) for m in marks) / args.steps
         for j, n in enumerate(names)}
 
@@ -416,7 +425,14 @@ def run_ours(args, world, rank, local):
     }
     if serial:
         line["block"] = "serial (h = x + Attn(LN1(x)), y = h + MLP(LN2(h)))"
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not serial:
+    if fp8:
+        line["dtype"] = "e4m3 GEMM operands (per-row scales), bf16 activations and attention"
+        line["gpu_launches"] = 5 * args.steps
+        fp8_peak = 2.0 * peak_sus  # nominal e4m3 / bf16 dense ratio 4.5 / 2.25
+        line["pct_of_peak"] = {"fp8_sustained_nominal_ratio": 100 * tflops / world / fp8_peak,
+                               "bf16_burst": 100 * tflops / world / peaks["bf16_tflops"],
+                               "source": f"{peak_src} bf16 x 2"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not serial and not fp8:
         f64 = oracle_sample(cfg, args.cpu_rows, seed_device="cuda")
         times = time_oracle(cfg, f64, args.cpu_rows, 1)
         cpu_v = args.cpu_rows / times[0]
@@ -436,6 +452,8 @@ def main():
     ap.add_argument("--workload", choices=["175b", "13b", "530b", "tiny", "swa"], default="175b")
     ap.add_argument("--block", choices=["ptb", "serial"], default="ptb",
                     help="the parallel block (default) or the serial block it replaces")
+    ap.add_argument("--precision", choices=["bf16", "fp8"], default="bf16",
+                    help="bf16 (default) or the variant with e4m3 GEMM operands")
     ap.add_argument("--cpu-rows", type=int, default=1024,
                     help="rows of the layer the CPU baseline computes (about 10 s of oracle work)")
     ap.add_argument("--ref-rows", type=int, default=64,

@@ -20,7 +20,8 @@ __all__ = [
     "PTBError", "load", "ptb_forward", "ptb_forward_events", "swa_attention",
     "swa_attention_strided", "swa_attention_counts", "layernorm", "gemm_qkv_up",
     "gemm_out_down", "gemm_workspace_size", "workspace_size", "release_workspace", "last_device_error",
-    "wait_probe", "serial_forward", "serial_workspace_size", "LIB_PATH", "SYMBOLS",
+    "wait_probe", "serial_forward", "serial_workspace_size", "prepare_fp8_weights",
+    "fp8_workspace_size", "ptb_forward_fp8", "LIB_PATH", "SYMBOLS",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libptb.so")
@@ -40,6 +41,9 @@ SYMBOLS = {
     "ptb_forward_events": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p, _p, _i32]),
     "ptb_release_workspace": (_st, []),
     "ptb_serial_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
+    "ptb_forward_fp8_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
+    "ptb_prepare_fp8_weights": (_st, [_p] * 4 + [_i64, _i64] + [_p] * 4 + [_p]),
+    "ptb_forward_fp8": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p]),
     "ptb_serial_forward": (_st, [_p] * 9 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p]),
     "ptb_forward_noalloc": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p]),
     "swa_attention": (_st, [_p, _p, _p, _i64, _i32, _i64, _i32, _i32, _f32, _p, _p]),
@@ -185,6 +189,49 @@ def serial_forward(x, ln1_gamma, ln1_beta, ln2_gamma, ln2_beta, w_qkv, w_o, w_up
                                 batch, seq, hidden, ffn, heads, window, _ptr(y), _ptr(workspace),
                                 ws_bytes, _stream(stream))
     _check(st, "ptb_serial_forward")
+    return y
+
+
+def prepare_fp8_weights(w_qkv, w_o, w_up, w_down, stream=None):
+    """Quantizes the layer's weights to e4m3 with one scale per output row;
+    returns (w1 [3H+F, H] uint8, s1 [3H+F] f32, w2 [H, H+F] uint8, s2 [H] f32)."""
+    lib = load()
+    for n, t in (("w_qkv", w_qkv), ("w_o", w_o), ("w_up", w_up), ("w_down", w_down)):
+        _bf16_cuda(n, t)
+    hidden, ffn = w_o.shape[0], w_up.shape[0]
+    dev = w_o.device
+    w1 = torch.empty(3 * hidden + ffn, hidden, dtype=torch.uint8, device=dev)
+    s1 = torch.empty(3 * hidden + ffn, dtype=torch.float32, device=dev)
+    w2 = torch.empty(hidden, hidden + ffn, dtype=torch.uint8, device=dev)
+    s2 = torch.empty(hidden, dtype=torch.float32, device=dev)
+    st = lib.ptb_prepare_fp8_weights(_ptr(w_qkv), _ptr(w_o), _ptr(w_up), _ptr(w_down), hidden,
+                                     ffn, _ptr(w1), _ptr(s1), _ptr(w2), _ptr(s2), _stream(stream))
+    _check(st, "ptb_prepare_fp8_weights")
+    return w1, s1, w2, s2
+
+
+def fp8_workspace_size(batch: int, seq: int, hidden: int, ffn: int) -> int:
+    return int(load().ptb_forward_fp8_workspace_size(batch, seq, hidden, ffn))
+
+
+def ptb_forward_fp8(x, ln_gamma, ln_beta, fp8_weights, heads: int, window: int, y=None,
+                    workspace=None, stream=None):
+    """The layer with e4m3 GEMM operands; fp8_weights from prepare_fp8_weights."""
+    lib = load()
+    w1, s1, w2, s2 = fp8_weights
+    for n, t in (("x", x), ("ln_gamma", ln_gamma), ("ln_beta", ln_beta)):
+        _bf16_cuda(n, t)
+    batch, seq, hidden = x.shape
+    ffn = w2.shape[1] - hidden
+    if y is None:
+        y = torch.empty_like(x)
+    ws_bytes = 0
+    if workspace is not None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.ptb_forward_fp8(_ptr(x), _ptr(ln_gamma), _ptr(ln_beta), _ptr(w1), _ptr(s1),
+                             _ptr(w2), _ptr(s2), batch, seq, hidden, ffn, heads, window, _ptr(y),
+                             _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "ptb_forward_fp8")
     return y
 
 

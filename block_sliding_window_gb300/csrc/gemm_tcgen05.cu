@@ -42,15 +42,20 @@ namespace ptb {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 64;  // bf16 elements in one 128-byte swizzle row
-constexpr int UMMA_K = 16;
+// One k-block is one 128-byte swizzle row: 64 bf16 or 128 e4m3 elements,
+// consumed by four MMAs (K = 16 bf16 or K = 32 e4m3 each, 32 bytes apart).
+template <bool FP8>
+struct Elem {
+  static constexpr int kBK = FP8 ? 128 : 64;
+};
+constexpr int kMmasPerBlock = 4;
 constexpr int kThreads = 192;
 
 template <int BN>
 struct Cfg {
   static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
-  static constexpr int kABytes = BM * BK * 2;
-  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kABytes = BM * 128;  // 128-byte rows: 64 bf16 or 128 e4m3
+  static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kBarBytes = 256;
@@ -95,6 +100,20 @@ __device__ __forceinline__ bool unit_at(const GemmArgs& p, int num_tiles, int nu
   return false;
 }
 
+// e4m3 operands carry one scale per A row and one per B row (= output
+// column): C[m, n] = a_scale[m] * b_scale[n] * sum_k A8[m, k] B8[n, k].
+__device__ __forceinline__ void dequantize(const GemmArgs& p, int row, int col, float (&acc)[32]) {
+  const float sa = row < p.M ? __ldg(p.a_scale + row) : 0.f;
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const float4 sb = __ldg(reinterpret_cast<const float4*>(p.b_scale + col) + v);
+    acc[4 * v] *= sa * sb.x;
+    acc[4 * v + 1] *= sa * sb.y;
+    acc[4 * v + 2] *= sa * sb.z;
+    acc[4 * v + 3] *= sa * sb.w;
+  }
+}
+
 // Epilogue of one 32-column chunk of one output row: acc (fp32) -> out (bf16).
 template <int EPI>
 __device__ __forceinline__ void store_chunk(const GemmArgs& p, int row, int col,
@@ -128,9 +147,10 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& p, int row, int col,
     dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs p) {
   using C = Cfg<BN>;
+  constexpr int BK = Elem<FP8>::kBK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -233,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16(BM, BN);
+      constexpr uint32_t idesc = FP8 ? umma_idesc_e4m3(BM, BN) : umma_idesc_bf16(BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -253,11 +273,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           const uint64_t adesc = sw128_kmajor_desc(smem_addr(stage_a(stage)));
           const uint64_t bdesc = sw128_kmajor_desc(smem_addr(stage_b(stage)));
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+          for (int kk = 0; kk < kMmasPerBlock; ++kk) {
             // +32 bytes along K inside the swizzled row = +2 in the
             // descriptor's 16-byte address units.
-            umma_bf16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc,
-                         (kb != u.kb0 || kk != 0) ? 1u : 0u);
+            const uint32_t accum = (kb != u.kb0 || kk != 0) ? 1u : 0u;
+            if constexpr (FP8)
+              umma_e4m3_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
+            else
+              umma_bf16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == C::kStages) {
@@ -323,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           float acc[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
+          if constexpr (FP8) dequantize(p, row, n0 + c, acc);
           if (row < p.M) store_chunk<EPI>(p, row, n0 + c, acc);
         }
       } else if (finish) {
@@ -346,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
               acc[4 * v + 3] += q.w;
             }
           }
+          if constexpr (FP8) dequantize(p, row, n0 + c, acc);
           if (row < p.M) store_chunk<EPI>(p, row, n0 + c, acc);
         }
       }
@@ -364,10 +389,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool FP8>
 cudaError_t launch_typed(const GemmArgs& a, cudaStream_t stream) {
   using C = Cfg<BN>;
-  auto kern = gemm_kernel<BN, EPI>;
+  auto kern = gemm_kernel<BN, EPI, FP8>;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -410,17 +435,33 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaMemsetAsync(a.counters, 0, a.split_r * 4 * sizeof(unsigned), stream);
     if (e != cudaSuccess) return e;
   }
+  if (a.fp8) {
+    if (a.epilogue == kEpiQkvGelu) {
+      switch (a.block_n) {
+        case 256: return launch_typed<256, kEpiQkvGelu, true>(a, stream);
+        case 128: return launch_typed<128, kEpiQkvGelu, true>(a, stream);
+        case 64: return launch_typed<64, kEpiQkvGelu, true>(a, stream);
+      }
+    } else {
+      switch (a.block_n) {
+        case 256: return launch_typed<256, kEpiResidual, true>(a, stream);
+        case 128: return launch_typed<128, kEpiResidual, true>(a, stream);
+        case 64: return launch_typed<64, kEpiResidual, true>(a, stream);
+      }
+    }
+    return cudaErrorInvalidValue;
+  }
   if (a.epilogue == kEpiQkvGelu) {
     switch (a.block_n) {
-      case 256: return launch_typed<256, kEpiQkvGelu>(a, stream);
-      case 128: return launch_typed<128, kEpiQkvGelu>(a, stream);
-      case 64: return launch_typed<64, kEpiQkvGelu>(a, stream);
+      case 256: return launch_typed<256, kEpiQkvGelu, false>(a, stream);
+      case 128: return launch_typed<128, kEpiQkvGelu, false>(a, stream);
+      case 64: return launch_typed<64, kEpiQkvGelu, false>(a, stream);
     }
   } else {
     switch (a.block_n) {
-      case 256: return launch_typed<256, kEpiResidual>(a, stream);
-      case 128: return launch_typed<128, kEpiResidual>(a, stream);
-      case 64: return launch_typed<64, kEpiResidual>(a, stream);
+      case 256: return launch_typed<256, kEpiResidual, false>(a, stream);
+      case 128: return launch_typed<128, kEpiResidual, false>(a, stream);
+      case 64: return launch_typed<64, kEpiResidual, false>(a, stream);
     }
   }
   return cudaErrorInvalidValue;

@@ -70,12 +70,14 @@ ptb_status device_state(DeviceState** out) {
 // 2-D bf16 tensor map over a row-major [outer, inner] matrix with row stride
 // `ld` elements, read in boxes of 64 (inner) x box_outer with 128-byte swizzle.
 bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
-              uint32_t box_outer) {
+              uint32_t box_outer, bool fp8 = false) {
+  // One box row is 128 bytes: 64 bf16 or 128 e4m3 elements.
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {ld * 2};
-  cuuint32_t box[2] = {64, box_outer};
+  cuuint64_t strides[1] = {ld * (fp8 ? 1 : 2)};
+  cuuint32_t box[2] = {fp8 ? 128u : 64u, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  return g_encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -137,10 +139,26 @@ bool head_dim_ok(int64_t d) { return d == 16 || d == 32 || d == 64 || d == 96 ||
 struct GemmSpec {
   const ptb_bf16 *a0, *a1, *b0, *b1;
   int64_t lda0, lda1, k0, k1, n0, n1;
+  // e4m3 operands (a0, b0 then point at bytes): one scale per A row and per B row.
+  bool fp8 = false;
+  const float* a_scale = nullptr;
+  const float* b_scale = nullptr;
   int64_t n() const { return n0 + n1; }
   int64_t k() const { return k0 + k1; }
+  int64_t kb() const { return k() / (fp8 ? 128 : 64); }
   int block_n() const { return n1 ? pick_block_n(n0, n1) : pick_block_n(n0, n0); }
 };
+
+GemmSpec spec_fp8(const void* a, int64_t lda, int64_t k, const void* b, int64_t n,
+                  const float* a_scale, const float* b_scale) {
+  GemmSpec g{static_cast<const ptb_bf16*>(a), static_cast<const ptb_bf16*>(a),
+             static_cast<const ptb_bf16*>(b), static_cast<const ptb_bf16*>(b), lda, lda, k, 0, n,
+             0};
+  g.fp8 = true;
+  g.a_scale = a_scale;
+  g.b_scale = b_scale;
+  return g;
+}
 
 GemmSpec spec_plain(const ptb_bf16* a, int64_t lda, int64_t k, const ptb_bf16* b, int64_t n) {
   return GemmSpec{a, a, b, b, lda, lda, k, 0, n, 0};
@@ -148,7 +166,7 @@ GemmSpec spec_plain(const ptb_bf16* a, int64_t lda, int64_t k, const ptb_bf16* b
 
 GemmPlan spec_plan(const GemmSpec& g, int64_t tokens, int sms) {
   const int bn = g.block_n() ? g.block_n() : 64;
-  return plan_gemm((tokens + 127) / 128 * (g.n() / bn), g.k() / 64, sms, bn);
+  return plan_gemm((tokens + 127) / 128 * (g.n() / bn), g.kb(), sms, bn);
 }
 
 ptb_status gemm_run(DeviceState* ds, const GemmSpec& g, int64_t tokens, ptb_bf16* out, int64_t ldo,
@@ -166,10 +184,10 @@ ptb_status gemm_run(DeviceState* ds, const GemmSpec& g, int64_t tokens, ptb_bf16
          make_map(&a.b0, g.b0, g.k0, N, g.k0, a.block_n) &&
          make_map(&a.b1, g.b1, g.k1, N, g.k1, a.block_n);
   } else {
-    ok = make_map(&a.a0, g.a0, K, tokens, g.lda0, 128) &&
-         make_map(&a.a1, g.a0, K, tokens, g.lda0, 128) &&
-         make_map(&a.b0, g.b0, K, g.n0, K, a.block_n) &&
-         make_map(&a.b1, g.n1 ? g.b1 : g.b0, K, g.n1 ? g.n1 : g.n0, K, a.block_n);
+    ok = make_map(&a.a0, g.a0, K, tokens, g.lda0, 128, g.fp8) &&
+         make_map(&a.a1, g.a0, K, tokens, g.lda0, 128, g.fp8) &&
+         make_map(&a.b0, g.b0, K, g.n0, K, a.block_n, g.fp8) &&
+         make_map(&a.b1, g.n1 ? g.b1 : g.b0, K, g.n1 ? g.n1 : g.n0, K, a.block_n, g.fp8);
   }
   if (!ok) return PTB_ERR_ARG;
   a.M = static_cast<int>(tokens);
@@ -183,8 +201,11 @@ ptb_status gemm_run(DeviceState* ds, const GemmSpec& g, int64_t tokens, ptb_bf16
   a.ld_resid = ldr;
   a.gelu_col = static_cast<int>(gelu_col);
   a.epilogue = resid ? kEpiResidual : kEpiQkvGelu;
+  a.fp8 = g.fp8 ? 1 : 0;
+  a.a_scale = g.a_scale;
+  a.b_scale = g.b_scale;
   const int64_t tiles = (tokens + 127) / 128 * (N / a.block_n);
-  apply_plan(a, tiles, K / 64, ds->sms, scratch, scratch_bytes);
+  apply_plan(a, tiles, g.kb(), ds->sms, scratch, scratch_bytes);
   a.status = ds->status;
   return launch_status(launch_gemm(a, stream));
 }
@@ -239,6 +260,15 @@ size_t serial_gemm_scratch(int64_t tokens, int64_t hidden, int64_t ffn, int sms)
     m = b > m ? b : m;
   }
   return m;
+}
+
+// Scratch for the split last waves of the FP8 layer's two GEMMs.
+size_t fp8_gemm_scratch(int64_t tokens, int64_t hidden, int64_t ffn, int sms) {
+  const GemmSpec g1 = spec_fp8(nullptr, hidden, hidden, nullptr, 3 * hidden + ffn, nullptr, nullptr);
+  const GemmSpec g2 = spec_fp8(nullptr, hidden + ffn, hidden + ffn, nullptr, hidden, nullptr, nullptr);
+  const size_t a = gemm_scratch_bytes(spec_plan(g1, tokens, sms));
+  const size_t b = gemm_scratch_bytes(spec_plan(g2, tokens, sms));
+  return a > b ? a : b;
 }
 
 ptb_status check_gemm_shape(int64_t tokens, int64_t hidden, int64_t ffn) {
@@ -696,6 +726,96 @@ ptb_status ptb_last_device_error(void) {
   if (cudaMemcpy(ds->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
     return PTB_ERR_LAUNCH;
   return static_cast<ptb_status>(word);
+}
+
+size_t ptb_forward_fp8_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn) {
+  if (batch < 1 || seq < 1 || hidden < 1 || ffn < 1) return 0;
+  const size_t t = static_cast<size_t>(batch) * static_cast<size_t>(seq);
+  size_t gemm = 0;
+  if (hidden % 64 == 0 && ffn % 64 == 0)
+    gemm = fp8_gemm_scratch(static_cast<int64_t>(t), hidden, ffn, current_sms());
+  return round_up(t * hidden, kAlign) + round_up(t * 4, kAlign) +
+         round_up(t * (3 * hidden + ffn) * 2, kAlign) + round_up(t * (hidden + ffn), kAlign) +
+         round_up(t * 4, kAlign) + gemm;
+}
+
+ptb_status ptb_prepare_fp8_weights(const ptb_bf16* w_qkv, const ptb_bf16* w_o,
+                                   const ptb_bf16* w_up, const ptb_bf16* w_down, int64_t hidden,
+                                   int64_t ffn, uint8_t* w1, float* s1, uint8_t* w2, float* s2,
+                                   ptb_stream stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const void* ptrs[] = {w_qkv, w_o, w_up, w_down, w1, s1, w2, s2};
+  for (const void* p : ptrs)
+    if (!p) return PTB_ERR_ARG;
+  for (const void* p : ptrs)
+    if (!aligned(p, 16)) return PTB_ERR_ALIGN;
+  if (hidden < 128 || ffn < 128) return PTB_ERR_ARG;
+  if (hidden % 128 || ffn % 128 || (hidden + ffn) * 2 > kQuantizeRowMaxBytes) return PTB_ERR_SHAPE;
+  DeviceState* ds = nullptr;
+  ptb_status st = device_state(&ds);
+  if (st != PTB_OK) return st;
+  const int h = static_cast<int>(hidden), f = static_cast<int>(ffn);
+  // w1 = [W_qkv ; W_up] row by row, w2 = [W_o | W_down] (rows concatenated along K).
+  if (launch_quantize_rows(bf(w_qkv), hidden, h, nullptr, 0, 0, 3 * hidden, 0, w1, s1, stream) !=
+          cudaSuccess ||
+      launch_quantize_rows(bf(w_up), hidden, h, nullptr, 0, 0, ffn, 3 * hidden, w1, s1, stream) !=
+          cudaSuccess ||
+      launch_quantize_rows(bf(w_o), hidden, h, bf(w_down), ffn, f, hidden, 0, w2, s2, stream) !=
+          cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  return PTB_OK;
+}
+
+ptb_status ptb_forward_fp8(const ptb_bf16* x, const ptb_bf16* ln_gamma, const ptb_bf16* ln_beta,
+                           const uint8_t* w1, const float* s1, const uint8_t* w2, const float* s2,
+                           int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
+                           int32_t window, ptb_bf16* y, void* workspace, size_t workspace_bytes,
+                           ptb_stream stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const void* ptrs[] = {x, ln_gamma, ln_beta, w1, s1, w2, s2, y};
+  ptb_status st = check_layer(ptrs, 8, batch, seq, hidden, ffn, heads, window);
+  if (st != PTB_OK) return st;
+  // e4m3 k-blocks are 128 elements; a quantized row is staged in shared memory.
+  if (hidden % 128 || ffn % 128 || (hidden + ffn) * 2 > kQuantizeRowMaxBytes) return PTB_ERR_SHAPE;
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != PTB_OK) return st;
+  const int64_t tokens = batch * seq;
+  const size_t need = ptb_forward_fp8_workspace_size(batch, seq, hidden, ffn);
+  st = acquire_workspace(ds, need, workspace, workspace_bytes, &workspace);
+  if (st != PTB_OK) return st;
+  char* p = static_cast<char*>(workspace);
+  uint8_t* xn8 = reinterpret_cast<uint8_t*>(p);
+  p += round_up(tokens * hidden, kAlign);
+  float* sx = reinterpret_cast<float*>(p);
+  p += round_up(tokens * 4, kAlign);
+  ptb_bf16* u = reinterpret_cast<ptb_bf16*>(p);
+  p += round_up(tokens * (3 * hidden + ffn) * 2, kAlign);
+  uint8_t* a8 = reinterpret_cast<uint8_t*>(p);
+  p += round_up(tokens * (hidden + ffn), kAlign);
+  float* sa = reinterpret_cast<float*>(p);
+  p += round_up(tokens * 4, kAlign);
+  const size_t scratch_size = need - static_cast<size_t>(p - static_cast<char*>(workspace));
+  const int64_t ldu = 3 * hidden + ffn;
+
+  // 1. xn8, sx = quantize(LN(x)) per token
+  if (launch_layernorm_fp8(bf(x), bf(ln_gamma), bf(ln_beta), tokens, static_cast<int>(hidden),
+                           1e-5f, xn8, sx, stream) != cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  // 2. U = [xn W_qkv^T | gelu(xn W_up^T)] from e4m3 operands
+  st = gemm_run(ds, spec_fp8(xn8, hidden, hidden, w1, ldu, sx, s1), tokens, u, ldu, nullptr, 0,
+                3 * hidden, p, scratch_size, stream);
+  if (st != PTB_OK) return st;
+  // 3. ctx = SWA(Q, K, V) over Q (bf16, as in ptb_forward)
+  if (launch_swa(swa_over_u(ds, u, ldu, batch, seq, hidden, heads, window), stream) != cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  // 4. a8, sa = quantize([ctx | G]) per token
+  if (launch_quantize_rows(bf(u), ldu, static_cast<int>(hidden), bf(u) + 3 * hidden, ldu,
+                           static_cast<int>(ffn), tokens, 0, a8, sa, stream) != cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  // 5. y = x + [ctx | G] [W_o | W_down]^T from e4m3 operands
+  return gemm_run(ds, spec_fp8(a8, hidden + ffn, hidden + ffn, w2, hidden, sa, s2), tokens, y,
+                  hidden, x, hidden, hidden, p, scratch_size, stream);
 }
 
 ptb_status ptb_wait_probe(uint64_t limit_ns, ptb_stream stream) {

@@ -40,10 +40,18 @@ struct GemmArgs {
   int split_s;          // pieces per remainder tile
   float* partials;      // [split_r * split_s][128][block_n] fp32
   unsigned* counters;   // [split_r][4] arrival counters, zeroed before each launch
+  // e4m3 operands (fp8 != 0): K counted in e4m3 elements, 128 per k-block;
+  // a_scale [M] and b_scale [N] dequantize the fp32 accumulator.
+  int fp8;
+  const float* a_scale;
+  const float* b_scale;
 };
 
 // Each K piece of a split tile keeps at least this many 64-wide k-blocks.
 constexpr int kMinSplitKBlocks = 8;
+// Largest bf16 row (bytes) the e4m3 row quantizer stages in shared memory:
+// the 227 KB opt-in block limit less room for its static reduction array.
+constexpr int64_t kQuantizeRowMaxBytes = 226 * 1024;
 
 struct GemmPlan {
   int grid, split_r, split_s;
@@ -77,6 +85,12 @@ cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* gamma,
                              const __nv_bfloat16* beta, int64_t rows, int hidden, float eps,
                              __nv_bfloat16* out, cudaStream_t stream);
 cudaError_t launch_swa(const SwaArgs& a, cudaStream_t stream);
+cudaError_t launch_layernorm_fp8(const __nv_bfloat16* x, const __nv_bfloat16* gamma,
+                                 const __nv_bfloat16* beta, int64_t rows, int hidden, float eps,
+                                 uint8_t* out, float* scale, cudaStream_t stream);
+cudaError_t launch_quantize_rows(const __nv_bfloat16* src0, int64_t ld0, int n0,
+                                 const __nv_bfloat16* src1, int64_t ld1, int n1, int64_t rows,
+                                 int64_t row0, uint8_t* out, float* scale, cudaStream_t stream);
 cudaError_t launch_wait_probe(uint64_t limit_ns, unsigned* status, cudaStream_t stream);
 
 }  // namespace ptb

@@ -169,6 +169,38 @@ ptb_status ptb_serial_forward(const ptb_bf16* x, const ptb_bf16* ln1_gamma,
                               int32_t window, ptb_bf16* y, void* workspace,
                               size_t workspace_bytes, ptb_stream stream);
 
+/*
+ * FP8 variant of ptb_forward.  The Megatron-LM page (mixed-precision
+ * section) lists FP8 among the supported precisions, to be used with dynamic
+ * scaling and with care for stability.  Both GEMMs take e4m3 operands with
+ * one dynamic fp32 scale per row of each operand:
+ *   xn8 = e4m3(LN(x) / sx), sx[t] = amax_t / 448   (per token)
+ *   A8  = e4m3([ctx | G] / sa), sa[t] per token    (second GEMM's input)
+ *   w1  = [W_qkv ; W_up] in e4m3 with s1[n] per output row   ([3H+F, H])
+ *   w2  = [W_o | W_down] in e4m3 with s2[n] per output row    ([H, H+F])
+ * and the accumulator is dequantized as sx[t] * s[n] * acc.  Attention, the
+ * GELU, the residual and all stored activations other than the two e4m3
+ * GEMM inputs stay bf16.  Accuracy is that of e4m3 (3 mantissa bits); the
+ * tests bound it by an exact computation with the same e4m3 rounding points.
+ *
+ * ptb_prepare_fp8_weights quantizes the bf16 weights once (w1, s1, w2, s2 are
+ * caller-owned device buffers of the sizes above; (H + F) * 2 <= 226 KiB).
+ * ptb_forward_fp8 then runs LN+quantize, the e4m3 [QKV | up] GEMM + GELU,
+ * SWA, a row quantization of [ctx | G], and the e4m3 [out | down] GEMM + x.
+ * Same shape rules, workspace and error conventions as ptb_forward, except
+ * that hidden and ffn must be multiples of 128 (one e4m3 k-block).
+ */
+size_t ptb_forward_fp8_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn);
+ptb_status ptb_prepare_fp8_weights(const ptb_bf16* w_qkv, const ptb_bf16* w_o,
+                                   const ptb_bf16* w_up, const ptb_bf16* w_down, int64_t hidden,
+                                   int64_t ffn, uint8_t* w1, float* s1, uint8_t* w2, float* s2,
+                                   ptb_stream stream);
+ptb_status ptb_forward_fp8(const ptb_bf16* x, const ptb_bf16* ln_gamma, const ptb_bf16* ln_beta,
+                           const uint8_t* w1, const float* s1, const uint8_t* w2, const float* s2,
+                           int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
+                           int32_t window, ptb_bf16* y, void* workspace, size_t workspace_bytes,
+                           ptb_stream stream);
+
 /* Frees the library's own workspace arena on the current device (if any). */
 ptb_status ptb_release_workspace(void);
 

@@ -73,3 +73,54 @@ def serial_bf16_storage(x, g1, b1, g2, b2, w_qkv, w_o, w_up, w_down, heads, wind
     h = bf16(x0[rows] + oracle.linear(bf16(ctx), w_o))
     g = bf16(oracle.gelu_tanh(oracle.linear(bf16(oracle.layer_norm(h, g2, b2)), w_up)))
     return bf16(h + oracle.linear(g, w_down))
+
+
+def e4m3_rows(a):
+    """Per-row e4m3 quantization as the FP8 path does it: scale = amax/448,
+    round to nearest e4m3 (saturating), dequantized back to float64."""
+    a = np.asarray(a, dtype=np.float64)
+    amax = np.abs(a).max(axis=-1, keepdims=True)
+    s = np.where(amax > 0, amax / 448.0, 1.0)
+    q = torch.from_numpy(np.clip(a / s, -448.0, 448.0).astype(np.float32)).to(torch.float8_e4m3fn)
+    return q.float().double().numpy() * s
+
+
+def e4m3_codes_fp32(a):
+    """Per-row e4m3 codes and scales computed in fp32, the precision in which
+    the FP8 path takes these decisions: s = amax / 448, code = the e4m3 value
+    nearest (ties to even) to v * (1 / s), clamped to +-448.  Returns (uint8
+    codes, float32 scales)."""
+    a = torch.as_tensor(a).float()
+    amax = a.abs().amax(dim=-1, keepdim=True)
+    s = torch.where(amax > 0, amax / torch.tensor(448.0), torch.ones_like(amax))
+    inv = torch.ones_like(s) / s
+    q = (a * inv).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8), s.squeeze(-1)
+
+
+def ptb_forward_fp8_storage(x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, heads, window, rows):
+    """The PTB with the FP8 path's rounding points: e4m3 xn, W1, [ctx | G] and
+    W2 (per-row scales), bf16 Q, K, V, P, ctx, G, y; exact arithmetic between."""
+    f = lambda t: t.detach().to("cpu").double().numpy() if hasattr(t, "detach") else np.asarray(t, np.float64)  # noqa: E731
+    x0 = f(x[0])
+    hidden = x0.shape[-1]
+    d = hidden // heads
+    w1 = e4m3_rows(np.concatenate([f(w_qkv), f(w_up)], axis=0))
+    w2 = e4m3_rows(np.concatenate([f(w_o), f(w_down)], axis=1))
+    kpos = oracle.needed_key_positions(rows, window)
+    need = np.union1d(kpos, rows)
+    xn = np.zeros_like(x0)
+    xn[need] = e4m3_rows(oracle.layer_norm(x0[need], ln_gamma, ln_beta))
+    q = bf16(xn[rows] @ w1[0:hidden].T)
+    k = bf16(xn[kpos] @ w1[hidden:2 * hidden].T)
+    v = bf16(xn[kpos] @ w1[2 * hidden:3 * hidden].T)
+    g = bf16(oracle.gelu_tanh(xn[rows] @ w1[3 * hidden:].T))
+    ctx = np.zeros((len(rows), hidden))
+    mask = oracle.band_mask(rows, kpos, window)
+    for h in range(heads):
+        sl = slice(h * d, (h + 1) * d)
+        sc = np.where(mask, (q[:, sl] @ k[:, sl].T) / math.sqrt(d), -np.inf)
+        e = np.exp(sc - sc.max(axis=1, keepdims=True))
+        ctx[:, sl] = (bf16(e) @ v[:, sl]) / e.sum(axis=1, keepdims=True)
+    a8 = e4m3_rows(np.concatenate([bf16(ctx), g], axis=1))
+    return bf16(x0[rows] + a8 @ w2.T)

@@ -16,7 +16,8 @@ import torch
 
 import oracle
 from block_sliding_window_gb300 import workloads
-from tests.bf16_storage_model import ptb_forward_bf16_storage, serial_bf16_storage
+from tests.bf16_storage_model import (e4m3_codes_fp32, ptb_forward_bf16_storage,
+                                     ptb_forward_fp8_storage, serial_bf16_storage)
 from tests.parity import MAX_ABS, REL_L2, assert_close, errors, to_np
 
 pytestmark = pytest.mark.gpu
@@ -224,6 +225,13 @@ def test_gemm_split_repeatable(ptb_lib):
     assert all(torch.equal(outs[0], o) for o in outs[1:])
 
 
+def test_fp8_rejects_shapes_off_the_128_grid(ptb_lib):
+    cfg = workloads.PTB_CONFIGS["tiny"]  # hidden 64
+    d = _cuda(workloads.ptb_inputs(cfg))
+    with pytest.raises(ptb_lib.PTBError):
+        ptb_lib.prepare_fp8_weights(d["w_qkv"], d["w_o"], d["w_up"], d["w_down"])
+
+
 def test_ptb_special_case_attention_off(ptb_lib):
     """W_o = 0 leaves y = x + MLP(LN(x)); W_down = 0 leaves y = x + Attn(LN(x))."""
     cfg = workloads.small_ptb(1, 200, 256, 4, 512, 33, seed=26)
@@ -280,6 +288,59 @@ def test_serial_forward_full_size_sampled(ptb_lib, name):
     print(f"serial {name}: rel-L2 {rel:.3e}, max-abs {mx:.3e}, beyond rounding {ex:.3e}, "
           f"bf16-storage floor {floor:.3e}, bound {bound:.3e}")
     assert rel <= REL_L2 and ex <= bound
+
+
+def _fp8_check(ptb_lib, cfg, host, d, rows, what):
+    """FP8 layer vs the fp64 oracle, bounded by 1.25x the error of an exact
+    computation with the same e4m3/bf16 rounding points (rel-L2 and max-abs)."""
+    w8 = ptb_lib.prepare_fp8_weights(d["w_qkv"], d["w_o"], d["w_up"], d["w_down"])
+    y = ptb_lib.ptb_forward_fp8(d["x"], d["ln_gamma"], d["ln_beta"], w8, cfg.heads, cfg.window)
+    torch.cuda.synchronize()
+    args = (host["x"], host["ln_gamma"], host["ln_beta"], host["w_qkv"], host["w_o"],
+            host["w_up"], host["w_down"], cfg.heads, cfg.window)
+    want = oracle.ptb_forward(*args, rows=rows)[0]
+    fl_rel, _, fl_ex = errors(ptb_forward_fp8_storage(*args, rows), want)
+    rel, mx, ex = errors(y[0, rows], want)
+    print(f"fp8 {what}: rel-L2 {rel:.3e} (floor {fl_rel:.3e}), max-abs beyond rounding {ex:.3e} "
+          f"(floor {fl_ex:.3e}), plain max-abs {mx:.3e}")
+    assert rel <= max(REL_L2, 1.25 * fl_rel), f"fp8 {what}: rel-L2 {rel:.3e}"
+    assert ex <= max(MAX_ABS, 1.25 * fl_ex), f"fp8 {what}: max-abs {ex:.3e}"
+
+
+@pytest.mark.parametrize("cfg", [c for c in SMALL_LAYERS if c.hidden % 128 == 0 and c.ffn % 128 == 0],
+                         ids=lambda c: c.name)
+def test_ptb_forward_fp8_small(ptb_lib, cfg):
+    host = workloads.ptb_inputs(cfg)
+    if cfg.batch != 1:
+        host["x"] = host["x"][:1]
+    d = _cuda(host)
+    _fp8_check(ptb_lib, cfg, host, d, list(range(cfg.seq)), cfg.name)
+
+
+def test_fp8_weight_codes_bit_exact(ptb_lib):
+    """The e4m3 weight codes and per-row scales are integer decisions taken in
+    fp32; they must match an fp32 CPU computation bit for bit."""
+    cfg = workloads.small_ptb(1, 64, 384, 4, 1536, 16, seed=27)
+    d = _cuda(workloads.ptb_inputs(cfg))
+    w1, s1, w2, s2 = ptb_lib.prepare_fp8_weights(d["w_qkv"], d["w_o"], d["w_up"], d["w_down"])
+    torch.cuda.synchronize()
+    c1, r1 = e4m3_codes_fp32(torch.cat([d["w_qkv"], d["w_up"]], 0).cpu())
+    c2, r2 = e4m3_codes_fp32(torch.cat([d["w_o"], d["w_down"]], 1).cpu())
+    assert torch.equal(s1.cpu(), r1) and torch.equal(s2.cpu(), r2)
+    assert torch.equal(w1.cpu(), c1) and torch.equal(w2.cpu(), c2)
+    # An all-zero row takes scale 1 and zero codes.
+    wz = d["w_up"].clone()
+    wz[5].zero_()
+    _, s1z, _, _ = ptb_lib.prepare_fp8_weights(d["w_qkv"], d["w_o"], wz, d["w_down"])
+    assert float(s1z[3 * cfg.hidden + 5]) == 1.0
+
+
+@pytest.mark.parametrize("name", ["13b"])
+def test_ptb_forward_fp8_full_size_sampled(ptb_lib, name):
+    cfg = workloads.PTB_CONFIGS[name]
+    d = workloads.ptb_inputs(cfg, device="cuda")
+    host = {k: v.cpu() for k, v in d.items()}
+    _fp8_check(ptb_lib, cfg, host, d, workloads.sample_rows(cfg.seq, cfg.window), name)
 
 
 @pytest.mark.parametrize("name", ["13b", "175b", "530b"])

@@ -40,3 +40,17 @@ def test_bf16_storage_model_sane():
     model0 = ptb_forward_bf16_storage(h["x"], h["ln_gamma"], h["ln_beta"], z["w_qkv"], z["w_o"],
                                       z["w_up"], z["w_down"], cfg.heads, cfg.window, rows)
     assert np.array_equal(model0, h["x"][0, rows].double().numpy())
+
+
+def test_e4m3_codes_known_values():
+    """e4m3 (1-4-3, bias 7, no infinities): 448 = 0x7E, 1.0 = 0x38, 2^-9 (the
+    smallest subnormal) = 0x01; an all-zero row takes scale 1."""
+    from tests.bf16_storage_model import e4m3_codes_fp32
+    codes, s = e4m3_codes_fp32(torch.tensor([[448.0, -448.0, 1.0, 2.0 ** -9, 0.0, -1.5],
+                                             [0.0, 0.0, 0.0, 0.0, 0.0, 0.0]]))
+    assert codes[0].tolist() == [0x7E, 0xFE, 0x38, 0x01, 0x00, 0xBC]
+    assert codes[1].tolist() == [0] * 6 and s.tolist() == [1.0, 1.0]
+    # amax maps to 448 and the scale is amax / 448; ties round to even:
+    # 17 lies halfway between the e4m3 values 16 and 18 and goes to 16.
+    codes, s = e4m3_codes_fp32(torch.tensor([[896.0, 34.0]]))
+    assert s.tolist() == [2.0] and codes[0].tolist() == [0x7E, 0x58]
