@@ -281,7 +281,8 @@ def run_swa(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    kern_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    per_step = [a.elapsed_time(b) for a, b in evs]
+    kern_ms = sum(per_step) / args.steps
     ms = max_over_ranks(kern_ms, world)
     band = sum(min(i + 1, cfg.window) for i in range(cfg.seq))
     tokens = cfg.batch * cfg.seq
@@ -296,6 +297,10 @@ def run_swa(args, world, rank, local):
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic", "config": config_json("swa", cfg, world),
             "tflops": flops / (ms * 1e-3) / 1e12,
+            "step_ms": {"mean": kern_ms, "median": statistics.median(per_step),
+                        "min": min(per_step)},
+            "tensor_frac_of_burst": flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "exp_per_s": cfg.batch * cfg.heads * band / (ms * 1e-3),
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": ach / peaks["hbm_gbs"], "peak_source": peak_src,
                          "traffic": traffic_for("swa_kernel", "swa", SWA_SRC)},
@@ -331,6 +336,9 @@ def run_ours(args, world, rank, local):
 
     def layer(x_in, marks=None):
         if fp8:
+            if marks is not None:
+                return bsw.ptb_forward_fp8_events(x_in, d["ln_gamma"], d["ln_beta"], w8,
+                                                  cfg.heads, cfg.window, marks, y=y, workspace=ws)
             return bsw.ptb_forward_fp8(x_in, d["ln_gamma"], d["ln_beta"], w8, cfg.heads,
                                        cfg.window, y=y, workspace=ws)
         if serial:  # second LayerNorm: gamma = 1, beta = 0 like the first
@@ -347,7 +355,9 @@ def run_ours(args, world, rank, local):
         raise RuntimeError("device status set during warm-up")
 
     # Timed region: K steps, per-kernel events recorded on the launching stream.
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    n_marks = 6 if fp8 else 5
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(n_marks)]
+             for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)  # sampled over the timed and the e2e regions
@@ -355,7 +365,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
-        layer(d["x"], None if (serial or fp8) else marks[i])
+        layer(d["x"], None if serial else marks[i])
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -364,10 +374,16 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device status {status} after the timed region")
     ms_local = t_start.elapsed_time(t_end) / args.steps
     ms = max_over_ranks(ms_local, world)
-    names = ["layernorm", "gemm_qkv_up", "swa", "gemm_out_down"]
-    per_kernel = None if (serial or fp8) else {
+    names = (["layernorm_quantize", "gemm_qkv_up", "swa", "quantize_ctx_g", "gemm_out_down"]
+             if fp8 else ["layernorm", "gemm_qkv_up", "swa", "gemm_out_down"])
+    per_kernel = None if serial else {
         n: sum(m[j].elapsed_time(m[j + 1]) for m in marks) / args.steps
         for j, n in enumerate(names)}
+    step_stats = None
+    if not serial:  # one step = first to last boundary event of that step
+        per_step = [m[0].elapsed_time(m[-1]) for m in marks]
+        step_stats = {"mean": sum(per_step) / len(per_step),
+                      "median": statistics.median(per_step), "min": min(per_step)}
 
     # End to end through the public call with host buffers: H2D of x, the
     # layer, D2H of y, every step.
@@ -408,6 +424,11 @@ def run_ours(args, world, rank, local):
                     "frac": g1_tf / peak_sus, "peak_source": f"{peak_src} bf16 sustained",
                     "traffic": traffic_for("gemm_qkv_up", args.workload, GEMM_SRC),
                     "algorithmic_flops_per_launch": fl["gemm1"]}
+        if fp8:  # e4m3 peak = measured bf16 sustained x the nominal 4.5 : 2.25 ratio
+            roofline.update(kernel="gemm_qkv_up (tcgen05 e4m3 [QKV|up] GEMM + GELU)",
+                            peak=2.0 * peak_sus, frac=g1_tf / (2.0 * peak_sus),
+                            peak_source=f"{peak_src} bf16 sustained x 2 (nominal e4m3:bf16)",
+                            traffic=traffic_for("fp8_gemm_qkv_up", args.workload, GEMM_SRC))
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -417,6 +438,7 @@ def run_ours(args, world, rank, local):
         "pct_of_peak": {"burst": 100 * tflops / world / peaks["bf16_tflops"],
                         "sustained": 100 * tflops / world / peak_sus, "source": peak_src},
         "kernels_ms": per_kernel,
+        "step_ms": step_stats,
         "roofline": roofline,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2},

@@ -21,7 +21,7 @@ __all__ = [
     "swa_attention_strided", "swa_attention_counts", "layernorm", "gemm_qkv_up",
     "gemm_out_down", "gemm_workspace_size", "workspace_size", "release_workspace", "last_device_error",
     "wait_probe", "serial_forward", "serial_workspace_size", "prepare_fp8_weights",
-    "fp8_workspace_size", "ptb_forward_fp8", "LIB_PATH", "SYMBOLS",
+    "fp8_workspace_size", "ptb_forward_fp8", "ptb_forward_fp8_events", "LIB_PATH", "SYMBOLS",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libptb.so")
@@ -44,6 +44,8 @@ SYMBOLS = {
     "ptb_forward_fp8_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
     "ptb_prepare_fp8_weights": (_st, [_p] * 4 + [_i64, _i64] + [_p] * 4 + [_p]),
     "ptb_forward_fp8": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p]),
+    "ptb_forward_fp8_events": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p, _p,
+                                                             _i32]),
     "ptb_serial_forward": (_st, [_p] * 9 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p]),
     "ptb_forward_noalloc": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p]),
     "swa_attention": (_st, [_p, _p, _p, _i64, _i32, _i64, _i32, _i32, _f32, _p, _p]),
@@ -214,25 +216,54 @@ def fp8_workspace_size(batch: int, seq: int, hidden: int, ffn: int) -> int:
     return int(load().ptb_forward_fp8_workspace_size(batch, seq, hidden, ffn))
 
 
-def ptb_forward_fp8(x, ln_gamma, ln_beta, fp8_weights, heads: int, window: int, y=None,
-                    workspace=None, stream=None):
-    """The layer with e4m3 GEMM operands; fp8_weights from prepare_fp8_weights."""
+def _fp8_layer(x, ln_gamma, ln_beta, fp8_weights, heads, window, y, workspace, stream, events):
     lib = load()
     w1, s1, w2, s2 = fp8_weights
     for n, t in (("x", x), ("ln_gamma", ln_gamma), ("ln_beta", ln_beta)):
         _bf16_cuda(n, t)
     batch, seq, hidden = x.shape
     ffn = w2.shape[1] - hidden
+    for n, t, dt, shape in (("w1", w1, torch.uint8, (3 * hidden + ffn, hidden)),
+                            ("s1", s1, torch.float32, (3 * hidden + ffn,)),
+                            ("w2", w2, torch.uint8, (hidden, hidden + ffn)),
+                            ("s2", s2, torch.float32, (hidden,))):
+        if t.dtype != dt or tuple(t.shape) != shape or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CUDA {dt} tensor of shape {shape}")
     if y is None:
         y = torch.empty_like(x)
     ws_bytes = 0
     if workspace is not None:
         ws_bytes = workspace.numel() * workspace.element_size()
-    st = lib.ptb_forward_fp8(_ptr(x), _ptr(ln_gamma), _ptr(ln_beta), _ptr(w1), _ptr(s1),
-                             _ptr(w2), _ptr(s2), batch, seq, hidden, ffn, heads, window, _ptr(y),
-                             _ptr(workspace), ws_bytes, _stream(stream))
-    _check(st, "ptb_forward_fp8")
+    args = (_ptr(x), _ptr(ln_gamma), _ptr(ln_beta), _ptr(w1), _ptr(s1), _ptr(w2), _ptr(s2), batch,
+            seq, hidden, ffn, heads, window, _ptr(y), _ptr(workspace), ws_bytes, _stream(stream))
+    if events is None:
+        _check(lib.ptb_forward_fp8(*args), "ptb_forward_fp8")
+        return y
+    if len(events) != 6:
+        raise ValueError("need 6 events")
+    st_obj = torch.cuda.current_stream() if stream is None else stream
+    for ev in events:
+        if not ev.cuda_event:  # torch creates the CUDA event on its first record
+            ev.record(st_obj)
+    handles = (ctypes.c_void_p * 6)(*[ev.cuda_event for ev in events])
+    _check(lib.ptb_forward_fp8_events(*args, handles, 6), "ptb_forward_fp8_events")
     return y
+
+
+def ptb_forward_fp8(x, ln_gamma, ln_beta, fp8_weights, heads: int, window: int, y=None,
+                    workspace=None, stream=None):
+    """The layer with e4m3 GEMM operands; fp8_weights from prepare_fp8_weights."""
+    return _fp8_layer(x, ln_gamma, ln_beta, fp8_weights, heads, window, y, workspace, stream,
+                      None)
+
+
+def ptb_forward_fp8_events(x, ln_gamma, ln_beta, fp8_weights, heads: int, window: int, events,
+                           y=None, workspace=None, stream=None):
+    """ptb_forward_fp8 that also records 6 torch.cuda.Event objects at the
+    kernel boundaries (before LN+quantize, GEMM1, SWA, quantize, GEMM2 and
+    after GEMM2)."""
+    return _fp8_layer(x, ln_gamma, ln_beta, fp8_weights, heads, window, y, workspace, stream,
+                      events)
 
 
 def swa_attention(q, k, v, window: int, scale: float = 0.0, o=None, stream=None):

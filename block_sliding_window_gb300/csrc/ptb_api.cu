@@ -766,17 +766,28 @@ ptb_status ptb_prepare_fp8_weights(const ptb_bf16* w_qkv, const ptb_bf16* w_o,
   return PTB_OK;
 }
 
-ptb_status ptb_forward_fp8(const ptb_bf16* x, const ptb_bf16* ln_gamma, const ptb_bf16* ln_beta,
-                           const uint8_t* w1, const float* s1, const uint8_t* w2, const float* s2,
-                           int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
-                           int32_t window, ptb_bf16* y, void* workspace, size_t workspace_bytes,
-                           ptb_stream stream_) {
+ptb_status ptb_forward_fp8_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
+                                  const ptb_bf16* ln_beta, const uint8_t* w1, const float* s1,
+                                  const uint8_t* w2, const float* s2, int64_t batch, int64_t seq,
+                                  int64_t hidden, int64_t ffn, int32_t heads, int32_t window,
+                                  ptb_bf16* y, void* workspace, size_t workspace_bytes,
+                                  ptb_stream stream_, void* const* events, int32_t n_events) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   const void* ptrs[] = {x, ln_gamma, ln_beta, w1, s1, w2, s2, y};
   ptb_status st = check_layer(ptrs, 8, batch, seq, hidden, ffn, heads, window);
   if (st != PTB_OK) return st;
   // e4m3 k-blocks are 128 elements; a quantized row is staged in shared memory.
   if (hidden % 128 || ffn % 128 || (hidden + ffn) * 2 > kQuantizeRowMaxBytes) return PTB_ERR_SHAPE;
+  if (events && n_events != 6) return PTB_ERR_ARG;
+  if (events)
+    for (int i = 0; i < 6; ++i)
+      if (!events[i]) return PTB_ERR_ARG;
+  auto mark = [&](int i) -> bool {
+    if (!events) return true;
+    if (cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) == cudaSuccess) return true;
+    cudaGetLastError();  // the failed record must not be reported by a later launch
+    return false;
+  };
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != PTB_OK) return st;
@@ -799,23 +810,40 @@ ptb_status ptb_forward_fp8(const ptb_bf16* x, const ptb_bf16* ln_gamma, const pt
   const int64_t ldu = 3 * hidden + ffn;
 
   // 1. xn8, sx = quantize(LN(x)) per token
+  if (!mark(0)) return PTB_ERR_ARG;
   if (launch_layernorm_fp8(bf(x), bf(ln_gamma), bf(ln_beta), tokens, static_cast<int>(hidden),
                            1e-5f, xn8, sx, stream) != cudaSuccess)
     return PTB_ERR_LAUNCH;
   // 2. U = [xn W_qkv^T | gelu(xn W_up^T)] from e4m3 operands
+  if (!mark(1)) return PTB_ERR_ARG;
   st = gemm_run(ds, spec_fp8(xn8, hidden, hidden, w1, ldu, sx, s1), tokens, u, ldu, nullptr, 0,
                 3 * hidden, p, scratch_size, stream);
   if (st != PTB_OK) return st;
   // 3. ctx = SWA(Q, K, V) over Q (bf16, as in ptb_forward)
+  if (!mark(2)) return PTB_ERR_ARG;
   if (launch_swa(swa_over_u(ds, u, ldu, batch, seq, hidden, heads, window), stream) != cudaSuccess)
     return PTB_ERR_LAUNCH;
   // 4. a8, sa = quantize([ctx | G]) per token
+  if (!mark(3)) return PTB_ERR_ARG;
   if (launch_quantize_rows(bf(u), ldu, static_cast<int>(hidden), bf(u) + 3 * hidden, ldu,
                            static_cast<int>(ffn), tokens, 0, a8, sa, stream) != cudaSuccess)
     return PTB_ERR_LAUNCH;
   // 5. y = x + [ctx | G] [W_o | W_down]^T from e4m3 operands
-  return gemm_run(ds, spec_fp8(a8, hidden + ffn, hidden + ffn, w2, hidden, sa, s2), tokens, y,
-                  hidden, x, hidden, hidden, p, scratch_size, stream);
+  if (!mark(4)) return PTB_ERR_ARG;
+  st = gemm_run(ds, spec_fp8(a8, hidden + ffn, hidden + ffn, w2, hidden, sa, s2), tokens, y,
+                hidden, x, hidden, hidden, p, scratch_size, stream);
+  if (st != PTB_OK) return st;
+  if (!mark(5)) return PTB_ERR_ARG;
+  return PTB_OK;
+}
+
+ptb_status ptb_forward_fp8(const ptb_bf16* x, const ptb_bf16* ln_gamma, const ptb_bf16* ln_beta,
+                           const uint8_t* w1, const float* s1, const uint8_t* w2, const float* s2,
+                           int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
+                           int32_t window, ptb_bf16* y, void* workspace, size_t workspace_bytes,
+                           ptb_stream stream) {
+  return ptb_forward_fp8_events(x, ln_gamma, ln_beta, w1, s1, w2, s2, batch, seq, hidden, ffn,
+                                heads, window, y, workspace, workspace_bytes, stream, nullptr, 0);
 }
 
 ptb_status ptb_wait_probe(uint64_t limit_ns, ptb_stream stream) {

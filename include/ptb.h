@@ -200,6 +200,19 @@ ptb_status ptb_forward_fp8(const ptb_bf16* x, const ptb_bf16* ln_gamma, const pt
                            int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
                            int32_t window, ptb_bf16* y, void* workspace, size_t workspace_bytes,
                            ptb_stream stream);
+/*
+ * ptb_forward_fp8 that also records six caller-owned CUDA events (cudaEvent_t
+ * passed as void*) on `stream`: before the LN + quantize kernel, the first
+ * GEMM, SWA, the row quantization and the second GEMM, and after the second
+ * GEMM.  n_events must be 6; a null event or a failed record returns
+ * PTB_ERR_ARG (kernels already enqueued stay queued).
+ */
+ptb_status ptb_forward_fp8_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
+                                  const ptb_bf16* ln_beta, const uint8_t* w1, const float* s1,
+                                  const uint8_t* w2, const float* s2, int64_t batch, int64_t seq,
+                                  int64_t hidden, int64_t ffn, int32_t heads, int32_t window,
+                                  ptb_bf16* y, void* workspace, size_t workspace_bytes,
+                                  ptb_stream stream, void* const* events, int32_t n_events);
 
 /* Frees the library's own workspace arena on the current device (if any). */
 ptb_status ptb_release_workspace(void);

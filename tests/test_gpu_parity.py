@@ -210,6 +210,20 @@ def test_ptb_forward_deterministic_and_events(ptb_lib):
         assert a.elapsed_time(b) >= 0.0
 
 
+def test_ptb_forward_fp8_deterministic_and_events(ptb_lib):
+    cfg = workloads.small_ptb(2, 300, 256, 4, 1024, 100, seed=21)
+    d = _cuda(workloads.ptb_inputs(cfg))
+    w8 = ptb_lib.prepare_fp8_weights(d["w_qkv"], d["w_o"], d["w_up"], d["w_down"])
+    args = (d["x"], d["ln_gamma"], d["ln_beta"], w8, cfg.heads, cfg.window)
+    y0 = ptb_lib.ptb_forward_fp8(*args)
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    y1 = ptb_lib.ptb_forward_fp8_events(*args, events)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1)
+    for a, b in zip(events, events[1:]):
+        assert a.elapsed_time(b) >= 0.0
+
+
 def test_gemm_split_repeatable(ptb_lib):
     """The split last wave gives the same bits call after call (the arrival
     order of the pieces does not change the summation order)."""

@@ -102,6 +102,18 @@ def test_ptb_forward_events_requires_five(lib):
     assert bsw.STATUS_NAMES[st] == "PTB_ERR_ARG"
 
 
+def test_ptb_forward_fp8_events_requires_six(lib):
+    import block_sliding_window_gb300 as bsw
+    ev = (ctypes.c_void_p * 6)()
+    st = lib.ptb_forward_fp8_events(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 128, 256, 4,
+                                    32, FAKE, None, 0, None, ev, 5)
+    assert bsw.STATUS_NAMES[st] == "PTB_ERR_ARG"
+    # six slots, one of them null
+    st = lib.ptb_forward_fp8_events(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 128, 256, 4,
+                                    32, FAKE, None, 0, None, ev, 6)
+    assert bsw.STATUS_NAMES[st] == "PTB_ERR_ARG"
+
+
 @pytest.mark.parametrize("d,w,seq,code", [(80, 8, 16, 2), (64, 0, 16, 1), (64, 4, 0, 1), (0, 4, 4, 2)])
 def test_swa_rejects_bad_arguments(lib, d, w, seq, code):
     st = lib.swa_attention(FAKE, FAKE, FAKE, 1, 2, seq, d, w, 0.0, FAKE * 2, None)
