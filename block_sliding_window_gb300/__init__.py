@@ -21,7 +21,9 @@ __all__ = [
     "swa_attention_strided", "swa_attention_counts", "layernorm", "gemm_qkv_up",
     "gemm_out_down", "gemm_workspace_size", "workspace_size", "release_workspace", "last_device_error",
     "wait_probe", "serial_forward", "serial_workspace_size", "prepare_fp8_weights",
-    "fp8_workspace_size", "ptb_forward_fp8", "ptb_forward_fp8_events", "LIB_PATH", "SYMBOLS",
+    "fp8_workspace_size", "ptb_forward_fp8", "ptb_forward_fp8_events", "train_saved_size",
+    "ptb_forward_train", "backward_workspace_size", "ptb_backward", "swa_attention_lse",
+    "swa_attention_backward", "LIB_PATH", "SYMBOLS",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libptb.so")
@@ -46,6 +48,14 @@ SYMBOLS = {
     "ptb_forward_fp8": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p]),
     "ptb_forward_fp8_events": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p, _p,
                                                              _i32]),
+    "ptb_train_saved_size": (_sz, [_i64, _i64, _i64, _i64, _i32]),
+    "ptb_forward_train": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p, _sz, _p]),
+    "ptb_backward_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i32]),
+    "ptb_backward": (_st, [_p] * 8 + [_sz] + [_i64] * 4 + [_i32, _i32] + [_p] * 8 + [_sz, _p]),
+    "swa_attention_lse": (_st, [_p, _p, _p, _i64, _i32, _i64, _i32, _i32, ctypes.c_float, _p, _p,
+                                _p]),
+    "swa_attention_backward": (_st, [_p] * 6 + [_i64, _i32, _i64, _i32, _i32, ctypes.c_float]
+                               + [_p] * 5),
     "ptb_serial_forward": (_st, [_p] * 9 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p]),
     "ptb_forward_noalloc": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p]),
     "swa_attention": (_st, [_p, _p, _p, _i64, _i32, _i64, _i32, _i32, _f32, _p, _p]),
@@ -311,6 +321,91 @@ def swa_attention_counts(q, k, v, window: int, scale: float = 0.0, stream=None):
                                   _ptr(o), _ptr(counts), _stream(stream))
     _check(st, "swa_attention_counts")
     return o, counts
+
+
+def train_saved_size(batch: int, seq: int, hidden: int, ffn: int, heads: int) -> int:
+    return int(load().ptb_train_saved_size(batch, seq, hidden, ffn, heads))
+
+
+def backward_workspace_size(batch: int, seq: int, hidden: int, ffn: int, heads: int) -> int:
+    return int(load().ptb_backward_workspace_size(batch, seq, hidden, ffn, heads))
+
+
+def ptb_forward_train(x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, heads: int, window: int,
+                      y=None, saved=None, workspace=None, stream=None):
+    """The layer forward that also keeps what ptb_backward needs; returns
+    (y, saved) with saved a uint8 CUDA tensor owned by the caller."""
+    lib = load()
+    (batch, seq, hidden, ffn), y, ws_bytes = _ptb_args(
+        x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, heads, window, y, workspace)
+    need = train_saved_size(batch, seq, hidden, ffn, heads)
+    if saved is None:
+        saved = torch.empty(need, dtype=torch.uint8, device=x.device)
+    st = lib.ptb_forward_train(_ptr(x), _ptr(ln_gamma), _ptr(ln_beta), _ptr(w_qkv), _ptr(w_o),
+                               _ptr(w_up), _ptr(w_down), batch, seq, hidden, ffn, heads, window,
+                               _ptr(y), _ptr(saved), saved.numel(), _ptr(workspace), ws_bytes,
+                               _stream(stream))
+    _check(st, "ptb_forward_train")
+    return y, saved
+
+
+def ptb_backward(dy, x, ln_gamma, w_qkv, w_o, w_up, w_down, saved, heads: int, window: int,
+                 grads=None, workspace=None, stream=None) -> dict:
+    """Gradients of the layer for upstream dy: dx (bf16) and fp32 dln_gamma,
+    dln_beta, dw_qkv, dw_o, dw_up, dw_down, returned as a dict (or written
+    into `grads`, a dict of preallocated tensors with those keys)."""
+    lib = load()
+    (batch, seq, hidden, ffn), _, ws_bytes = _ptb_args(
+        x, ln_gamma, ln_gamma, w_qkv, w_o, w_up, w_down, heads, window, dy, workspace)
+    if tuple(dy.shape) != tuple(x.shape):
+        raise ValueError("dy must have the shape of x")
+    if grads is None:
+        dev, f32 = x.device, torch.float32
+        grads = dict(dx=torch.empty_like(x),
+                     dln_gamma=torch.empty(hidden, dtype=f32, device=dev),
+                     dln_beta=torch.empty(hidden, dtype=f32, device=dev),
+                     dw_qkv=torch.empty(3 * hidden, hidden, dtype=f32, device=dev),
+                     dw_o=torch.empty(hidden, hidden, dtype=f32, device=dev),
+                     dw_up=torch.empty(ffn, hidden, dtype=f32, device=dev),
+                     dw_down=torch.empty(hidden, ffn, dtype=f32, device=dev))
+    g = grads
+    st = lib.ptb_backward(_ptr(dy), _ptr(x), _ptr(ln_gamma), _ptr(w_qkv), _ptr(w_o), _ptr(w_up),
+                          _ptr(w_down), _ptr(saved), saved.numel(), batch, seq, hidden, ffn, heads,
+                          window, _ptr(g["dx"]), _ptr(g["dln_gamma"]), _ptr(g["dln_beta"]),
+                          _ptr(g["dw_qkv"]), _ptr(g["dw_o"]), _ptr(g["dw_up"]),
+                          _ptr(g["dw_down"]), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "ptb_backward")
+    return g
+
+
+def swa_attention_lse(q, k, v, window: int, scale: float = 0.0, stream=None):
+    """swa_attention that also returns the per-row base-2 log-sum-exp:
+    (o, lse[B, heads, s] fp32)."""
+    lib = load()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _bf16_cuda(n, t)
+    b, h, s, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((b, h, s), dtype=torch.float32, device=q.device)
+    st = lib.swa_attention_lse(_ptr(q), _ptr(k), _ptr(v), b, h, s, d, window, scale, _ptr(o),
+                               _ptr(lse), _stream(stream))
+    _check(st, "swa_attention_lse")
+    return o, lse
+
+
+def swa_attention_backward(q, k, v, o, dout, lse, window: int, scale: float = 0.0, stream=None):
+    """Gradients (dq, dk, dv) of swa_attention for the upstream dout."""
+    lib = load()
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _bf16_cuda(n, t)
+    b, h, s, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty((b, h, s), dtype=torch.float32, device=q.device)
+    st = lib.swa_attention_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), b,
+                                    h, s, d, window, scale, _ptr(dq), _ptr(dk), _ptr(dv),
+                                    _ptr(delta), _stream(stream))
+    _check(st, "swa_attention_backward")
+    return dq, dk, dv
 
 
 def layernorm(x, gamma, beta, eps: float = 1e-5, out=None, stream=None):

@@ -114,16 +114,75 @@ __device__ __forceinline__ void dequantize(const GemmArgs& p, int row, int col, 
   }
 }
 
-// Epilogue of one 32-column chunk of one output row: acc (fp32) -> out (bf16).
+// d/dz gelu_tanh(z) = 0.5 (1 + t) + 0.5 z (1 - t^2) c (1 + 3 a z^2),
+// t = tanh(c (z + a z^3)), c = sqrt(2 / pi), a = 0.044715.
+__device__ __forceinline__ float gelu_tanh_grad(float z) {
+  const float k0 = 0.7978845608028654f;
+  const float k1 = 0.044715f;
+  const float t = tanhf(k0 * (z + k1 * z * z * z));
+  return 0.5f * (1.0f + t) + 0.5f * z * (1.0f - t * t) * k0 * (1.0f + 3.0f * k1 * z * z);
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst_row, const uint32_t (&packed)[16]) {
+  uint4* dst = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+  for (int v = 0; v < 4; ++v)
+    dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+}
+
+// Epilogue of one 32-column chunk of one output row: acc (fp32) -> out.
 template <int EPI>
 __device__ __forceinline__ void store_chunk(const GemmArgs& p, int row, int col,
                                             const float (&acc)[32]) {
+  // Destination region (a 32-column chunk never straddles a split point).
+  void* base = p.out;
+  int64_t ld = p.ld_out;
+  int64_t r = row, c = col;
+  if (col >= p.out_split_col) {
+    base = p.out1;
+    ld = p.ld_out1;
+    c -= p.out_split_col;
+  } else if (row >= p.out_split_row) {
+    base = p.out1;
+    ld = p.ld_out1;
+    r -= p.out_split_row;
+  }
+  if constexpr (EPI == kEpiF32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + r * ld + c);
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+      dst[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+    return;
+  }
   uint32_t packed[16];
   if constexpr (EPI == kEpiQkvGelu) {
     if (col >= p.gelu_col) {
+      if (p.aux) {  // keep the pre-activation for the backward pass
+#pragma unroll
+        for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
+        store_bf16x32(p.aux + row * p.ld_aux + (col - p.gelu_col), packed);
+      }
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         packed[j] = pack_bf16x2(gelu_tanh(acc[2 * j]), gelu_tanh(acc[2 * j + 1]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
+    }
+  } else if constexpr (EPI == kEpiDgelu) {
+    if (col >= p.gelu_col) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.aux + row * p.ld_aux + (col - p.gelu_col));
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint4 z = __ldg(src + v);
+        const uint32_t zs[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int e = v * 8 + j * 2;
+          packed[v * 4 + j] = pack_bf16x2(acc[e] * gelu_tanh_grad(bf16_lo(zs[j])),
+                                          acc[e + 1] * gelu_tanh_grad(bf16_hi(zs[j])));
+        }
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
@@ -141,16 +200,30 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& p, int row, int col,
       }
     }
   }
-  uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.ld_out + col);
-#pragma unroll
-  for (int v = 0; v < 4; ++v)
-    dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+  store_bf16x32(static_cast<__nv_bfloat16*>(base) + r * ld + c, packed);
 }
 
-template <int BN, int EPI, bool FP8>
+// Output tile origin of tile index t (M index fastest, or N index fastest).
+__device__ __forceinline__ void tile_origin(const GemmArgs& p, int t, int num_m, int num_n, int bn,
+                                            int& m0, int& n0) {
+  if (p.n_fastest) {
+    m0 = (t / num_n) * BM;
+    n0 = (t % num_n) * bn;
+  } else {
+    m0 = (t % num_m) * BM;
+    n0 = (t / num_m) * bn;
+  }
+}
+
+template <int BN, int EPI, bool FP8, int LAYOUT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs p) {
   using C = Cfg<BN>;
   constexpr int BK = Elem<FP8>::kBK;
+  // MN-major operands arrive as 64-wide MN blocks of 64 K rows (8 KB each).
+  constexpr bool kAmn = (LAYOUT & 1) != 0;
+  constexpr bool kBmn = (LAYOUT & 2) != 0;
+  constexpr uint32_t kMnBlock = 64 * 128;
+  static_assert(!(FP8 && LAYOUT != kLayoutKK), "e4m3 operands are K-major only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -167,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const int num_m = (p.M + BM - 1) / BM;
   const int num_n = p.N / BN;
   const int num_tiles = num_m * num_n;
-  const int num_kb = p.K / BK;
+  const int num_kb = (p.K + BK - 1) / BK;  // a K tail is zero-filled by TMA
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -203,13 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
-      // L2 priorities (measured): the weights are streamed once, so they go
-      // first; the first GEMM's A (xn, re-read by every N tile) stays.  Giving
-      // the weights normal priority slowed the 175B layer by 11%, and an L2
-      // prefetch of the tiles 8 k-blocks ahead by 48%.
-      const uint64_t pol = p.epilogue == kEpiQkvGelu ? l2_policy_evict_last()
-                                                     : l2_policy_evict_first();
-      const uint64_t pol_b = l2_policy_evict_first();
+      // L2 priorities (measured on the forward GEMMs): the operand that is
+      // streamed once goes first, the one re-read by later tiles stays.
+      // Giving the forward weights normal priority slowed the 175B layer by
+      // 11%, and an L2 prefetch of the tiles 8 k-blocks ahead by 48%.
+      const uint64_t pol = p.a_keep ? l2_policy_evict_last() : l2_policy_evict_first();
+      const uint64_t pol_b = p.b_keep ? l2_policy_evict_last() : l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0;  // bit s: stage s has had a load issued
@@ -217,8 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       bool ok = true;
       Unit u;
       for (int i = 0; ok && unit_at(p, num_tiles, num_kb, i, u); ++i) {
-        const int m0 = (u.tile % num_m) * BM;
-        const int n0 = (u.tile / num_m) * BN;
+        int m0, n0;
+        tile_origin(p, u.tile, num_m, num_n, BN, m0, n0);
         const bool nlo = n0 < p.n_split;
         const int by = nlo ? n0 : n0 - p.n_split;
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
@@ -230,9 +302,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           const bool klo = k < p.k_split;
           const int kx = klo ? k : k - p.k_split;
           mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
-          tma_load_2d(stage_a(stage), klo ? &p.a0 : &p.a1, &full_bar[stage], kx, m0, pol);
-          tma_load_2d(stage_b(stage), (nlo && klo) ? &p.b0 : &p.b1, &full_bar[stage], kx, by,
-                      pol_b);
+          const CUtensorMap* amap = klo ? &p.a0 : &p.a1;
+          const CUtensorMap* bmap = (nlo && klo) ? &p.b0 : &p.b1;
+          if constexpr (kAmn) {
+#pragma unroll
+            for (int h = 0; h < BM / 64; ++h)
+              tma_load_2d(stage_a(stage) + h * kMnBlock, amap, &full_bar[stage], m0 + 64 * h, kx,
+                          pol);
+          } else {
+            tma_load_2d(stage_a(stage), amap, &full_bar[stage], kx, m0, pol);
+          }
+          if constexpr (kBmn) {
+#pragma unroll
+            for (int h = 0; h < BN / 64; ++h)
+              tma_load_2d(stage_b(stage) + h * kMnBlock, bmap, &full_bar[stage], by + 64 * h, kx,
+                          pol_b);
+          } else {
+            tma_load_2d(stage_b(stage), bmap, &full_bar[stage], kx, by, pol_b);
+          }
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == C::kStages) {
@@ -253,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      constexpr uint32_t idesc = FP8 ? umma_idesc_e4m3(BM, BN) : umma_idesc_bf16(BM, BN);
+      constexpr uint32_t idesc = (FP8 ? umma_idesc_e4m3(BM, BN) : umma_idesc_bf16(BM, BN)) |
+                                 (kAmn ? 1u << 15 : 0u) | (kBmn ? 1u << 16 : 0u);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -270,17 +358,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = sw128_kmajor_desc(smem_addr(stage_a(stage)));
-          const uint64_t bdesc = sw128_kmajor_desc(smem_addr(stage_b(stage)));
+          const uint64_t adesc = kAmn ? sw128_mnmajor_desc(smem_addr(stage_a(stage)), kMnBlock)
+                                      : sw128_kmajor_desc(smem_addr(stage_a(stage)));
+          const uint64_t bdesc = kBmn ? sw128_mnmajor_desc(smem_addr(stage_b(stage)), kMnBlock)
+                                      : sw128_kmajor_desc(smem_addr(stage_b(stage)));
+          // One MMA step along K: +32 bytes inside a K-major swizzled row
+          // (+2 in the descriptor's 16-byte units), or 16 rows of 128 bytes
+          // of an MN-major block (+128).
+          constexpr uint64_t kStepA = kAmn ? 128 : 2;
+          constexpr uint64_t kStepB = kBmn ? 128 : 2;
 #pragma unroll
           for (int kk = 0; kk < kMmasPerBlock; ++kk) {
-            // +32 bytes along K inside the swizzled row = +2 in the
-            // descriptor's 16-byte address units.
             const uint32_t accum = (kb != u.kb0 || kk != 0) ? 1u : 0u;
             if constexpr (FP8)
-              umma_e4m3_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
+              umma_e4m3_ss(d_tmem, adesc + kStepA * kk, bdesc + kStepB * kk, idesc, accum);
             else
-              umma_bf16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
+              umma_bf16_ss(d_tmem, adesc + kStepA * kk, bdesc + kStepB * kk, idesc, accum);
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == C::kStages) {
@@ -305,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const uint32_t acc_phase = (i >> 1) & 1;
       if (!mbar_wait_warp(&tfull_bar[acc_buf], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
-      const int m0 = (u.tile % num_m) * BM;
-      const int n0 = (u.tile / num_m) * BN;
+      int m0, n0;
+      tile_origin(p, u.tile, num_m, num_n, BN, m0, n0);
       const int row = m0 + row_local;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc_buf * BN);
@@ -389,10 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   }
 }
 
-template <int BN, int EPI, bool FP8>
+template <int BN, int EPI, bool FP8, int LAYOUT>
 cudaError_t launch_typed(const GemmArgs& a, cudaStream_t stream) {
   using C = Cfg<BN>;
-  auto kern = gemm_kernel<BN, EPI, FP8>;
+  auto kern = gemm_kernel<BN, EPI, FP8, LAYOUT>;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -430,40 +523,44 @@ GemmPlan plan_gemm(int64_t tiles, int64_t num_kb, int sms, int block_n) {
   return g;
 }
 
+namespace {
+
+template <int EPI, bool FP8, int LAYOUT>
+cudaError_t launch_bn(const GemmArgs& a, cudaStream_t stream) {
+  switch (a.block_n) {
+    case 256: return launch_typed<256, EPI, FP8, LAYOUT>(a, stream);
+    case 128: return launch_typed<128, EPI, FP8, LAYOUT>(a, stream);
+    case 64: return launch_typed<64, EPI, FP8, LAYOUT>(a, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (a.split_s >= 2 && a.split_r > 0) {
     cudaError_t e = cudaMemsetAsync(a.counters, 0, a.split_r * 4 * sizeof(unsigned), stream);
     if (e != cudaSuccess) return e;
   }
-  if (a.fp8) {
-    if (a.epilogue == kEpiQkvGelu) {
-      switch (a.block_n) {
-        case 256: return launch_typed<256, kEpiQkvGelu, true>(a, stream);
-        case 128: return launch_typed<128, kEpiQkvGelu, true>(a, stream);
-        case 64: return launch_typed<64, kEpiQkvGelu, true>(a, stream);
-      }
-    } else {
-      switch (a.block_n) {
-        case 256: return launch_typed<256, kEpiResidual, true>(a, stream);
-        case 128: return launch_typed<128, kEpiResidual, true>(a, stream);
-        case 64: return launch_typed<64, kEpiResidual, true>(a, stream);
-      }
-    }
+  // The instantiated (epilogue, operand type, layout) combinations: the
+  // forward GEMMs (bf16 and e4m3, K-major) and the backward GEMMs (bf16).
+  if (a.layout == kLayoutKK) {
+    if (a.epilogue == kEpiQkvGelu)
+      return a.fp8 ? launch_bn<kEpiQkvGelu, true, kLayoutKK>(a, stream)
+                   : launch_bn<kEpiQkvGelu, false, kLayoutKK>(a, stream);
+    if (a.epilogue == kEpiResidual)
+      return a.fp8 ? launch_bn<kEpiResidual, true, kLayoutKK>(a, stream)
+                   : launch_bn<kEpiResidual, false, kLayoutKK>(a, stream);
     return cudaErrorInvalidValue;
   }
-  if (a.epilogue == kEpiQkvGelu) {
-    switch (a.block_n) {
-      case 256: return launch_typed<256, kEpiQkvGelu, false>(a, stream);
-      case 128: return launch_typed<128, kEpiQkvGelu, false>(a, stream);
-      case 64: return launch_typed<64, kEpiQkvGelu, false>(a, stream);
-    }
-  } else {
-    switch (a.block_n) {
-      case 256: return launch_typed<256, kEpiResidual, false>(a, stream);
-      case 128: return launch_typed<128, kEpiResidual, false>(a, stream);
-      case 64: return launch_typed<64, kEpiResidual, false>(a, stream);
-    }
+  if (a.fp8) return cudaErrorInvalidValue;
+  if (a.layout == kLayoutKN) {
+    if (a.epilogue == kEpiDgelu) return launch_bn<kEpiDgelu, false, kLayoutKN>(a, stream);
+    if (a.epilogue == kEpiF32) return launch_bn<kEpiF32, false, kLayoutKN>(a, stream);
+    return cudaErrorInvalidValue;
   }
+  if (a.layout == kLayoutNN && a.epilogue == kEpiF32)
+    return launch_bn<kEpiF32, false, kLayoutNN>(a, stream);
   return cudaErrorInvalidValue;
 }
 

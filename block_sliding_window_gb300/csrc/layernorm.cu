@@ -9,6 +9,8 @@
 // squares are reduced in fp32 (warp shuffles, then across warps through shared
 // memory), and the normalised row is written with 16-byte stores.  The kernel
 // is a pure HBM stream: 2 * H bytes read and H * 2 bytes written per row.
+// With `stats` set it also keeps (mean, 1/sqrt(var + eps)) of every row for
+// the backward pass.
 #include "ptb_device.cuh"
 
 namespace ptb {
@@ -34,7 +36,7 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
     const __nv_bfloat16* __restrict__ beta, int hidden, float eps,
-    __nv_bfloat16* __restrict__ out) {
+    __nv_bfloat16* __restrict__ out, float2* __restrict__ stats) {
   __shared__ float red[kLnThreads / 32];
   const int64_t row = blockIdx.x;
   const int nvec = hidden / 8;
@@ -70,6 +72,7 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(
   }
   const float var = block_sum(sq, red) / static_cast<float>(hidden);
   const float rstd = rsqrtf(var + eps);
+  if (stats && threadIdx.x == 0) stats[row] = make_float2(mean, rstd);
 
   const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
   const uint4* b4 = reinterpret_cast<const uint4*>(beta);
@@ -99,12 +102,12 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(
 
 cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* gamma,
                              const __nv_bfloat16* beta, int64_t rows, int hidden, float eps,
-                             __nv_bfloat16* out, cudaStream_t stream) {
+                             __nv_bfloat16* out, cudaStream_t stream, float2* stats) {
   if (hidden % 8 != 0 || hidden / 8 > kLnMaxVec * kLnThreads) return cudaErrorInvalidValue;
   if (rows <= 0) return cudaSuccess;
   if (rows > 0x7fffffff) return cudaErrorInvalidValue;
   layernorm_kernel<<<static_cast<unsigned>(rows), kLnThreads, 0, stream>>>(x, gamma, beta, hidden,
-                                                                           eps, out);
+                                                                           eps, out, stats);
   return cudaGetLastError();
 }
 

@@ -171,7 +171,8 @@ GemmPlan spec_plan(const GemmSpec& g, int64_t tokens, int sms) {
 
 ptb_status gemm_run(DeviceState* ds, const GemmSpec& g, int64_t tokens, ptb_bf16* out, int64_t ldo,
                     const ptb_bf16* resid, int64_t ldr, int64_t gelu_col, void* scratch,
-                    size_t scratch_bytes, cudaStream_t stream) {
+                    size_t scratch_bytes, cudaStream_t stream, ptb_bf16* aux = nullptr,
+                    int64_t ld_aux = 0) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.block_n = g.block_n();
@@ -195,8 +196,20 @@ ptb_status gemm_run(DeviceState* ds, const GemmSpec& g, int64_t tokens, ptb_bf16
   a.K = static_cast<int>(K);
   a.n_split = static_cast<int>(g.n1 ? g.n0 : N);
   a.k_split = static_cast<int>(g.k1 ? g.k0 : K);
+  a.layout = kLayoutKK;
+  a.n_fastest = 0;
+  // The first GEMM re-reads xn for every N tile; the weights and the second
+  // GEMM's A are streamed.
+  a.a_keep = resid ? 0 : 1;
+  a.b_keep = 0;
   a.out = bf(out);
   a.ld_out = ldo;
+  a.out1 = a.out;
+  a.ld_out1 = ldo;
+  a.out_split_col = static_cast<int>(N);
+  a.out_split_row = static_cast<int>(tokens);
+  a.aux = aux ? bf(aux) : nullptr;
+  a.ld_aux = ld_aux;
   a.resid = resid ? bf(resid) : nullptr;
   a.ld_resid = ldr;
   a.gelu_col = static_cast<int>(gelu_col);
@@ -236,6 +249,105 @@ ptb_status gemm_out_down(DeviceState* ds, const ptb_bf16* ctx, int64_t ld_ctx, c
                          ptb_bf16* y, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
   return gemm_run(ds, spec_out_down(ctx, ld_ctx, g, ld_g, w_o, w_down, hidden, ffn), tokens, y,
                   hidden, x, hidden, hidden, scratch, scratch_bytes, stream);
+}
+
+// A GEMM of the backward pass, C[M, N] = A[M, K] B[N, K]^T, with operands
+// read in place from row-major matrices:
+//   A K-major:  a_i stored [M, K_i] (row stride lda_i);  A MN-major: [K_i, M].
+//   B K-major:  b_i stored [N_i, K] or [N, K_i];  B MN-major: [K, N_i] or [K_i, N].
+// A and B may be split in two along K at k_split (a0/b0 before, a1/b1
+// after), or B along N at n_split; at most one split (0 = none).
+struct GemmCall {
+  int layout = kLayoutKK;
+  int epilogue = kEpiF32;
+  int64_t M = 0, N = 0, K = 0;
+  const ptb_bf16 *a0 = nullptr, *a1 = nullptr, *b0 = nullptr, *b1 = nullptr;
+  int64_t lda0 = 0, lda1 = 0, ldb0 = 0, ldb1 = 0;
+  int64_t k_split = 0, n_split = 0;
+  void* out = nullptr;
+  int64_t ld_out = 0;
+  void* out1 = nullptr;
+  int64_t ld_out1 = 0;
+  int64_t out_split_col = 0, out_split_row = 0;  // 0 = no split
+  ptb_bf16* aux = nullptr;
+  int64_t ld_aux = 0;
+  int64_t gelu_col = 0;
+  bool a_keep = false, b_keep = false;
+  int block_n() const {
+    return n_split ? pick_block_n(n_split, N - n_split) : pick_block_n(N, N);
+  }
+  int64_t tiles() const {
+    const int bn = block_n() ? block_n() : 64;
+    return (M + 127) / 128 * (N / bn);
+  }
+  int64_t kb() const { return (K + 63) / 64; }
+};
+
+// 2-D bf16 tensor map with boxes of 64 x 64 over a row-major [outer, inner]
+// matrix (an MN-major operand: inner = M or N, outer = K).
+bool make_map_mn(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld) {
+  return make_map(map, base, inner, outer, ld, 64);
+}
+
+size_t call_scratch(const GemmCall& c, int sms) {
+  const int bn = c.block_n() ? c.block_n() : 64;
+  return gemm_scratch_bytes(plan_gemm(c.tiles(), c.kb(), sms, bn));
+}
+
+ptb_status gemm_call(DeviceState* ds, const GemmCall& c, void* scratch, size_t scratch_bytes,
+                     cudaStream_t stream) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.block_n = c.block_n();
+  if (!a.block_n || c.M < 1 || c.K < 1 || c.M > (1 << 30) || c.N > (1 << 30) || c.K > (1 << 30))
+    return PTB_ERR_SHAPE;
+  if ((c.k_split && c.n_split) || c.k_split % 64 || c.n_split % 64) return PTB_ERR_SHAPE;
+  const bool amn = (c.layout & 1) != 0, bmn = (c.layout & 2) != 0;
+  const int64_t k0 = c.k_split ? c.k_split : c.K, k1 = c.k_split ? c.K - c.k_split : 0;
+  const int64_t n0 = c.n_split ? c.n_split : c.N, n1 = c.n_split ? c.N - c.n_split : 0;
+  const ptb_bf16* a1 = c.k_split ? c.a1 : c.a0;
+  const int64_t lda1 = c.k_split ? c.lda1 : c.lda0;
+  const ptb_bf16* b1 = (c.k_split || c.n_split) ? c.b1 : c.b0;
+  const int64_t ldb1 = (c.k_split || c.n_split) ? c.ldb1 : c.ldb0;
+  const int64_t ka1 = k1 ? k1 : k0;
+  bool ok;
+  if (amn)
+    ok = make_map_mn(&a.a0, c.a0, c.M, k0, c.lda0) && make_map_mn(&a.a1, a1, c.M, ka1, lda1);
+  else
+    ok = make_map(&a.a0, c.a0, k0, c.M, c.lda0, 128) && make_map(&a.a1, a1, ka1, c.M, lda1, 128);
+  // B: the K extent of source i is its K part under a K split, else K; the
+  // N extent is its N part under an N split, else N.
+  const int64_t bk0 = c.k_split ? k0 : c.K, bk1 = c.k_split ? k1 : c.K;
+  const int64_t bn0 = c.n_split ? n0 : c.N, bn1 = c.n_split ? n1 : c.N;
+  if (bmn)
+    ok = ok && make_map_mn(&a.b0, c.b0, bn0, bk0, c.ldb0) && make_map_mn(&a.b1, b1, bn1, bk1, ldb1);
+  else
+    ok = ok && make_map(&a.b0, c.b0, bk0, bn0, c.ldb0, a.block_n) &&
+         make_map(&a.b1, b1, bk1, bn1, ldb1, a.block_n);
+  if (!ok) return PTB_ERR_ARG;
+  a.M = static_cast<int>(c.M);
+  a.N = static_cast<int>(c.N);
+  a.K = static_cast<int>(c.K);
+  a.n_split = static_cast<int>(c.n_split ? c.n_split : c.N);
+  a.k_split = static_cast<int>(c.k_split ? c.k_split : c.K);
+  a.layout = c.layout;
+  a.epilogue = c.epilogue;
+  const int64_t num_m = (c.M + 127) / 128, num_n = c.N / a.block_n;
+  a.n_fastest = num_m > num_n ? 1 : 0;
+  a.a_keep = c.a_keep ? 1 : 0;
+  a.b_keep = c.b_keep ? 1 : 0;
+  a.out = c.out;
+  a.ld_out = c.ld_out;
+  a.out1 = c.out1 ? c.out1 : c.out;
+  a.ld_out1 = c.out1 ? c.ld_out1 : c.ld_out;
+  a.out_split_col = static_cast<int>(c.out_split_col ? c.out_split_col : c.N);
+  a.out_split_row = static_cast<int>(c.out_split_row ? c.out_split_row : c.M);
+  a.aux = c.aux ? bf(c.aux) : nullptr;
+  a.ld_aux = c.ld_aux;
+  a.gelu_col = static_cast<int>(c.gelu_col ? c.gelu_col : c.N);
+  apply_plan(a, c.tiles(), c.kb(), ds->sms, scratch, scratch_bytes);
+  a.status = ds->status;
+  return launch_status(launch_gemm(a, stream));
 }
 
 // Scratch for the split last waves of the PTB's two GEMMs (the larger one).
@@ -447,6 +559,145 @@ SwaArgs swa_over_u(DeviceState* ds, ptb_bf16* u, int64_t ldu, int64_t batch, int
   sa.status = ds->status;
   sa.sms = ds->sms;
   return sa;
+}
+
+// Saved activations of ptb_forward_train, in this order, each region
+// starting on a kAlign boundary.
+struct SavedLayout {
+  size_t xn, stats, u, z, ctx, lse, total;
+};
+
+SavedLayout saved_layout(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int64_t heads) {
+  const size_t t = static_cast<size_t>(batch) * static_cast<size_t>(seq);
+  SavedLayout l;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += round_up(bytes, kAlign);
+    return at;
+  };
+  l.xn = take(t * hidden * 2);
+  l.stats = take(t * 8);
+  l.u = take(t * (3 * hidden + ffn) * 2);
+  l.z = take(t * ffn * 2);
+  l.ctx = take(t * hidden * 2);
+  l.lse = take(static_cast<size_t>(batch) * heads * seq * 4);
+  l.total = off;
+  return l;
+}
+
+// The four GEMMs of the backward pass (pointers left null: for sizing).
+GemmCall call_dgrad_out(int64_t t, int64_t h, int64_t f) {  // [dctx | dG] = dy [W_o | W_down]
+  GemmCall c;
+  c.layout = kLayoutKN;
+  c.epilogue = kEpiDgelu;
+  c.M = t, c.N = h + f, c.K = h, c.n_split = h;
+  c.lda0 = h, c.ldb0 = h, c.ldb1 = f;
+  c.out_split_col = h, c.gelu_col = h;
+  c.a_keep = true;
+  return c;
+}
+GemmCall call_wgrad_out(int64_t t, int64_t h, int64_t f, int64_t ldu) {  // dy^T [ctx | G]
+  GemmCall c;
+  c.layout = kLayoutNN;
+  c.epilogue = kEpiF32;
+  c.M = h, c.N = h + f, c.K = t, c.n_split = h;
+  c.lda0 = h, c.ldb0 = h, c.ldb1 = ldu;
+  c.out_split_col = h;
+  c.a_keep = true;
+  return c;
+}
+GemmCall call_dgrad_in(int64_t t, int64_t h, int64_t f, int64_t ldu) {  // dU1 [W_qkv ; W_up]
+  GemmCall c;
+  c.layout = kLayoutKN;
+  c.epilogue = kEpiF32;
+  c.M = t, c.N = h, c.K = ldu, c.k_split = 3 * h;
+  c.lda0 = ldu, c.lda1 = ldu, c.ldb0 = h, c.ldb1 = h;
+  (void)f;
+  return c;
+}
+GemmCall call_wgrad_in(int64_t t, int64_t h, int64_t f, int64_t ldu) {  // dU1^T xn
+  GemmCall c;
+  c.layout = kLayoutNN;
+  c.epilogue = kEpiF32;
+  c.M = ldu, c.N = h, c.K = t;
+  c.lda0 = ldu, c.ldb0 = h;
+  c.out_split_row = 3 * h;
+  c.b_keep = true;
+  (void)f;
+  return c;
+}
+
+struct BwdLayout {
+  size_t dctx, du1, delta, dxn, ln_part, gemm, total;
+};
+
+BwdLayout bwd_layout(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int64_t heads,
+                     int sms) {
+  const int64_t t = batch * seq, ldu = 3 * hidden + ffn;
+  BwdLayout l;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += round_up(bytes, kAlign);
+    return at;
+  };
+  l.dctx = take(static_cast<size_t>(t) * hidden * 2);
+  l.du1 = take(static_cast<size_t>(t) * ldu * 2);
+  l.delta = take(static_cast<size_t>(batch) * heads * seq * 4);
+  l.dxn = take(static_cast<size_t>(t) * hidden * 4);
+  l.ln_part = take(static_cast<size_t>(ln_backward_chunks(t)) * 2 * hidden * 4);
+  size_t g = 0;
+  for (const GemmCall& c : {call_dgrad_out(t, hidden, ffn), call_wgrad_out(t, hidden, ffn, ldu),
+                            call_dgrad_in(t, hidden, ffn, ldu), call_wgrad_in(t, hidden, ffn, ldu)}) {
+    const size_t b = call_scratch(c, sms);
+    g = b > g ? b : g;
+  }
+  l.gemm = take(g);
+  l.total = off;
+  return l;
+}
+
+ptb_status check_saved(const void* saved, size_t saved_bytes, const SavedLayout& l) {
+  if (!saved) return PTB_ERR_ARG;
+  if (!aligned(saved, kAlign)) return PTB_ERR_ALIGN;
+  if (saved_bytes < l.total) return PTB_ERR_WORKSPACE;
+  return PTB_OK;
+}
+
+SwaBwdArgs swa_bwd_args(DeviceState* ds, const ptb_bf16* u, const ptb_bf16* ctx,
+                        const ptb_bf16* dctx, ptb_bf16* du1, const float* lse, float* delta,
+                        int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
+                        int32_t window) {
+  const int64_t d = hidden / heads, ldu = 3 * hidden + ffn;
+  SwaBwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = bf(u);
+  a.k = bf(u) + hidden;
+  a.v = bf(u) + 2 * hidden;
+  a.o = bf(ctx);
+  a.dout = bf(dctx);
+  a.dq = bf(du1);
+  a.dk = bf(du1) + hidden;
+  a.dv = bf(du1) + 2 * hidden;
+  a.q_sb = a.k_sb = a.v_sb = a.dq_sb = a.dk_sb = a.dv_sb = seq * ldu;
+  a.q_sh = a.k_sh = a.v_sh = a.dq_sh = a.dk_sh = a.dv_sh = d;
+  a.q_ss = a.k_ss = a.v_ss = a.dq_ss = a.dk_ss = a.dv_ss = ldu;
+  a.o_sb = a.do_sb = seq * hidden;
+  a.o_sh = a.do_sh = d;
+  a.o_ss = a.do_ss = hidden;
+  a.lse = lse;
+  a.delta = delta;
+  a.batch = static_cast<int>(batch);
+  a.heads = heads;
+  a.seq = static_cast<int>(seq);
+  a.head_dim = static_cast<int>(d);
+  a.window = window;
+  a.scale = 1.0f / std::sqrt(static_cast<float>(d));
+  a.scale_log2 = a.scale * 1.4426950408889634f;
+  a.status = ds->status;
+  a.sms = ds->sms;
+  return a;
 }
 
 }  // namespace
@@ -844,6 +1095,206 @@ ptb_status ptb_forward_fp8(const ptb_bf16* x, const ptb_bf16* ln_gamma, const pt
                            ptb_stream stream) {
   return ptb_forward_fp8_events(x, ln_gamma, ln_beta, w1, s1, w2, s2, batch, seq, hidden, ffn,
                                 heads, window, y, workspace, workspace_bytes, stream, nullptr, 0);
+}
+
+size_t ptb_train_saved_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,
+                            int32_t heads) {
+  if (batch < 1 || seq < 1 || hidden < 1 || ffn < 1 || heads < 1) return 0;
+  return saved_layout(batch, seq, hidden, ffn, heads).total;
+}
+
+ptb_status ptb_forward_train(const ptb_bf16* x, const ptb_bf16* ln_gamma, const ptb_bf16* ln_beta,
+                             const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
+                             const ptb_bf16* w_down, int64_t batch, int64_t seq, int64_t hidden,
+                             int64_t ffn, int32_t heads, int32_t window, ptb_bf16* y, void* saved,
+                             size_t saved_bytes, void* workspace, size_t workspace_bytes,
+                             ptb_stream stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const void* ptrs[] = {x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, y};
+  ptb_status st = check_layer(ptrs, 8, batch, seq, hidden, ffn, heads, window);
+  if (st != PTB_OK) return st;
+  const SavedLayout l = saved_layout(batch, seq, hidden, ffn, heads);
+  st = check_saved(saved, saved_bytes, l);
+  if (st != PTB_OK) return st;
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != PTB_OK) return st;
+  const int64_t tokens = batch * seq, ldu = 3 * hidden + ffn;
+  const size_t need = layer_gemm_scratch(tokens, hidden, ffn, ds->sms);
+  st = acquire_workspace(ds, need, workspace, workspace_bytes, &workspace);
+  if (st != PTB_OK) return st;
+  char* sv = static_cast<char*>(saved);
+  ptb_bf16* xn = reinterpret_cast<ptb_bf16*>(sv + l.xn);
+  float2* stats = reinterpret_cast<float2*>(sv + l.stats);
+  ptb_bf16* u = reinterpret_cast<ptb_bf16*>(sv + l.u);
+  ptb_bf16* z = reinterpret_cast<ptb_bf16*>(sv + l.z);
+  ptb_bf16* ctx = reinterpret_cast<ptb_bf16*>(sv + l.ctx);
+  float* lse = reinterpret_cast<float*>(sv + l.lse);
+  // 1. xn = LN(x), keeping (mean, rstd) per token
+  if (launch_layernorm(bf(x), bf(ln_gamma), bf(ln_beta), tokens, static_cast<int>(hidden), 1e-5f,
+                       bf(xn), stream, stats) != cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  // 2. U = [xn W_qkv^T | gelu(Z)], Z = xn W_up^T kept
+  st = gemm_run(ds, spec_qkv_up(xn, w_qkv, w_up, hidden, ffn), tokens, u, ldu, nullptr, 0,
+                3 * hidden, workspace, need, stream, z, ffn);
+  if (st != PTB_OK) return st;
+  // 3. ctx = SWA(Q, K, V) into its own buffer (Q is needed again), with the
+  //    per-row log-sum-exp
+  SwaArgs sa = swa_over_u(ds, u, ldu, batch, seq, hidden, heads, window);
+  sa.o = bf(ctx);
+  sa.o_sb = seq * hidden;
+  sa.o_ss = hidden;
+  sa.lse = lse;
+  if (launch_swa(sa, stream) != cudaSuccess) return PTB_ERR_LAUNCH;
+  // 4. y = x + [ctx | G] [W_o | W_down]^T
+  return gemm_out_down(ds, ctx, hidden, u + 3 * hidden, ldu, w_o, w_down, x, tokens, hidden, ffn,
+                       y, workspace, need, stream);
+}
+
+size_t ptb_backward_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,
+                                   int32_t heads) {
+  if (batch < 1 || seq < 1 || hidden < 64 || ffn < 64 || heads < 1) return 0;
+  if (hidden % 64 || ffn % 64) return 0;
+  return bwd_layout(batch, seq, hidden, ffn, heads, current_sms()).total;
+}
+
+ptb_status ptb_backward(const ptb_bf16* dy, const ptb_bf16* x, const ptb_bf16* ln_gamma,
+                        const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
+                        const ptb_bf16* w_down, const void* saved, size_t saved_bytes,
+                        int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
+                        int32_t window, ptb_bf16* dx, float* dln_gamma, float* dln_beta,
+                        float* dw_qkv, float* dw_o, float* dw_up, float* dw_down, void* workspace,
+                        size_t workspace_bytes, ptb_stream stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const void* ptrs[] = {dy, x, ln_gamma, w_qkv, w_o, w_up, w_down, dx,
+                        dln_gamma, dln_beta, dw_qkv, dw_o, dw_up, dw_down};
+  ptb_status st = check_layer(ptrs, 14, batch, seq, hidden, ffn, heads, window);
+  if (st != PTB_OK) return st;
+  const SavedLayout l = saved_layout(batch, seq, hidden, ffn, heads);
+  st = check_saved(saved, saved_bytes, l);
+  if (st != PTB_OK) return st;
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != PTB_OK) return st;
+  const BwdLayout w = bwd_layout(batch, seq, hidden, ffn, heads, ds->sms);
+  st = acquire_workspace(ds, w.total, workspace, workspace_bytes, &workspace);
+  if (st != PTB_OK) return st;
+  const int64_t t = batch * seq, ldu = 3 * hidden + ffn;
+  const char* sv = static_cast<const char*>(saved);
+  const ptb_bf16* xn = reinterpret_cast<const ptb_bf16*>(sv + l.xn);
+  const float2* stats = reinterpret_cast<const float2*>(sv + l.stats);
+  const ptb_bf16* u = reinterpret_cast<const ptb_bf16*>(sv + l.u);
+  const ptb_bf16* z = reinterpret_cast<const ptb_bf16*>(sv + l.z);
+  const ptb_bf16* ctx = reinterpret_cast<const ptb_bf16*>(sv + l.ctx);
+  const float* lse = reinterpret_cast<const float*>(sv + l.lse);
+  char* ws = static_cast<char*>(workspace);
+  ptb_bf16* dctx = reinterpret_cast<ptb_bf16*>(ws + w.dctx);
+  ptb_bf16* du1 = reinterpret_cast<ptb_bf16*>(ws + w.du1);
+  float* delta = reinterpret_cast<float*>(ws + w.delta);
+  float* dxn = reinterpret_cast<float*>(ws + w.dxn);
+  float* ln_part = reinterpret_cast<float*>(ws + w.ln_part);
+  void* scratch = ws + w.gemm;
+  const size_t scratch_bytes = w.total - w.gemm;
+
+  // 1. [dctx | dZ] = dy [W_o | W_down], dZ = dG * gelu'(Z) written into dU1
+  GemmCall c = call_dgrad_out(t, hidden, ffn);
+  c.a0 = dy, c.b0 = w_o, c.b1 = w_down;
+  c.out = dctx, c.ld_out = hidden, c.out1 = du1 + 3 * hidden, c.ld_out1 = ldu;
+  c.aux = const_cast<ptb_bf16*>(z), c.ld_aux = ffn;
+  st = gemm_call(ds, c, scratch, scratch_bytes, stream);
+  if (st != PTB_OK) return st;
+  // 2. [dW_o | dW_down] = dy^T [ctx | G]
+  c = call_wgrad_out(t, hidden, ffn, ldu);
+  c.a0 = dy, c.b0 = ctx, c.b1 = u + 3 * hidden;
+  c.out = dw_o, c.ld_out = hidden, c.out1 = dw_down, c.ld_out1 = ffn;
+  st = gemm_call(ds, c, scratch, scratch_bytes, stream);
+  if (st != PTB_OK) return st;
+  // 3. [dQ | dK | dV] into dU1 from the banded attention backward
+  if (launch_swa_backward(swa_bwd_args(ds, u, ctx, dctx, du1, lse, delta, batch, seq, hidden, ffn,
+                                       heads, window),
+                          stream) != cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  // 4. dxn = dU1 [W_qkv ; W_up]   (fp32)
+  c = call_dgrad_in(t, hidden, ffn, ldu);
+  c.a0 = du1, c.a1 = du1 + 3 * hidden, c.b0 = w_qkv, c.b1 = w_up;
+  c.out = dxn, c.ld_out = hidden;
+  st = gemm_call(ds, c, scratch, scratch_bytes, stream);
+  if (st != PTB_OK) return st;
+  // 5. [dW_qkv ; dW_up] = dU1^T xn
+  c = call_wgrad_in(t, hidden, ffn, ldu);
+  c.a0 = du1, c.b0 = xn;
+  c.out = dw_qkv, c.ld_out = hidden, c.out1 = dw_up, c.ld_out1 = hidden;
+  st = gemm_call(ds, c, scratch, scratch_bytes, stream);
+  if (st != PTB_OK) return st;
+  // 6. dx = dy + LN backward of dxn; dgamma, dbeta
+  return launch_status(launch_layernorm_backward(bf(x), bf(ln_gamma), stats, dxn, bf(dy), t,
+                                                 static_cast<int>(hidden), bf(dx), dln_gamma,
+                                                 dln_beta, ln_part, stream));
+}
+
+ptb_status swa_attention_lse(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v,
+                             int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
+                             int32_t window, float scale, ptb_bf16* o, float* lse,
+                             ptb_stream stream) {
+  if (!lse || !aligned(lse, 4)) return PTB_ERR_ARG;
+  if (batch < 1 || seq < 1 || heads < 1) return PTB_ERR_ARG;
+  if (batch > 65535 || seq > (1ll << 30)) return PTB_ERR_SHAPE;
+  if (o == q || o == k || o == v) return PTB_ERR_ARG;
+  SwaArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = bf(q), a.k = bf(k), a.v = bf(v), a.o = bf(o);
+  const int64_t ss = head_dim, sh = seq * head_dim, sb = heads * seq * head_dim;
+  a.q_sb = a.k_sb = a.v_sb = a.o_sb = sb;
+  a.q_sh = a.k_sh = a.v_sh = a.o_sh = sh;
+  a.q_ss = a.k_ss = a.v_ss = a.o_ss = ss;
+  a.batch = static_cast<int>(batch);
+  a.heads = heads;
+  a.seq = static_cast<int>(seq);
+  a.head_dim = head_dim;
+  a.window = window;
+  a.lse = lse;
+  return swa_impl(a, scale, static_cast<cudaStream_t>(stream));
+}
+
+ptb_status swa_attention_backward(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v,
+                                  const ptb_bf16* o, const ptb_bf16* dout, const float* lse,
+                                  int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
+                                  int32_t window, float scale, ptb_bf16* dq, ptb_bf16* dk,
+                                  ptb_bf16* dv, float* delta, ptb_stream stream) {
+  const void* ptrs[] = {q, k, v, o, dout, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!p) return PTB_ERR_ARG;
+  if (!lse || !delta || batch < 1 || seq < 1 || heads < 1 || window < 1) return PTB_ERR_ARG;
+  if (!head_dim_ok(head_dim)) return PTB_ERR_SHAPE;
+  if (batch > 65535 || seq > (1ll << 30) || batch * static_cast<int64_t>(heads) > 65535)
+    return PTB_ERR_SHAPE;
+  for (const void* p : ptrs)
+    if (!aligned(p, 16)) return PTB_ERR_ALIGN;
+  if (!aligned(lse, 4) || !aligned(delta, 4)) return PTB_ERR_ALIGN;
+  if (scale < 0.f || !std::isfinite(scale)) return PTB_ERR_ARG;
+  DeviceState* ds = nullptr;
+  ptb_status st = device_state(&ds);
+  if (st != PTB_OK) return st;
+  SwaBwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = bf(q), a.k = bf(k), a.v = bf(v), a.o = bf(o), a.dout = bf(dout);
+  a.dq = bf(dq), a.dk = bf(dk), a.dv = bf(dv);
+  const int64_t ss = head_dim, sh = seq * head_dim, sb = heads * seq * head_dim;
+  a.q_sb = a.k_sb = a.v_sb = a.o_sb = a.do_sb = a.dq_sb = a.dk_sb = a.dv_sb = sb;
+  a.q_sh = a.k_sh = a.v_sh = a.o_sh = a.do_sh = a.dq_sh = a.dk_sh = a.dv_sh = sh;
+  a.q_ss = a.k_ss = a.v_ss = a.o_ss = a.do_ss = a.dq_ss = a.dk_ss = a.dv_ss = ss;
+  a.lse = lse;
+  a.delta = delta;
+  a.batch = static_cast<int>(batch);
+  a.heads = heads;
+  a.seq = static_cast<int>(seq);
+  a.head_dim = head_dim;
+  a.window = window;
+  a.scale = scale == 0.f ? 1.0f / std::sqrt(static_cast<float>(head_dim)) : scale;
+  a.scale_log2 = a.scale * 1.4426950408889634f;
+  a.status = ds->status;
+  a.sms = ds->sms;
+  return launch_status(launch_swa_backward(a, static_cast<cudaStream_t>(stream)));
 }
 
 ptb_status ptb_wait_probe(uint64_t limit_ns, ptb_stream stream) {

@@ -1,0 +1,589 @@
+// Backward pass of causal sliding-window attention (SWA) on tcgen05 tensor
+// cores.
+//
+// For o_i = sum_j P_ij v_j with P = softmax over the band of q_i.k_j * scale
+// (row i sees keys max(0, i-w+1) .. i; MegaScale study notes, ch.2 §2.2, SWA
+// row) and an upstream gradient dO, the chain rule gives, with
+// delta_i = sum_c dO_ic o_ic = sum_j P_ij (dO_i . v_j):
+//   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - delta),
+//   dQ = scale * dS K,   dK = scale * dS^T Q.
+// P is recomputed from the scores and the forward pass's per-row log-sum-exp
+// (base 2): P_ij = 2^(q_i.k_j * scale * log2 e - lse2_i).
+//
+// Two persistent kernels, so that no gradient is summed with atomics:
+//   kKV  one item = 128 keys of one (batch entry, head): stationary K and V
+//        tiles, moving 64-query tiles of Q and dO over the keys' band
+//          S^T  = K Q^T,   dP^T = V dO^T      (M 128 keys, N 64, K d)
+//          dV  += P^T dO,  dK  += dS^T Q      (M 128, N d, K 64 queries)
+//   kQ   one item = 128 queries: stationary Q and dO, moving 64-key tiles
+//          S = Q K^T,  dP = dO V^T            (M 128 queries, N 64, K d)
+//          dQ += dS K                         (M 128, N d, K 64 keys)
+// Roles (192 threads): warp 0 TMA, warp 1 TMEM owner and MMA issuer, warps
+// 2..5 one stationary row per thread (TMEM lane = row): recompute P and dS
+// for the tile in fp32, write them as bf16 operand rows into shared memory
+// (128-byte-swizzled K-major layout, two buffers), and at the end of an item
+// read the fp32 accumulators from TMEM and store bf16 gradients.  The
+// moving tiles are read twice, once as K-major and once as MN-major operands
+// of the same shared-memory copy.
+// Every mbarrier wait is bounded (see mbar_wait); on a timeout all roles
+// unwind, wait for their own copies and MMAs, free TMEM and return.
+#include "ptb_device.cuh"
+
+namespace ptb {
+namespace {
+
+constexpr int BR = 128;  // stationary rows per item (= MMA M)
+constexpr int BC = 64;   // moving rows per tile (= N of the score MMAs)
+constexpr int kThreads = 192;
+constexpr int kKV = 0;   // dK, dV kernel
+constexpr int kQ = 1;    // dQ kernel
+
+template <int D, int MODE>
+struct BwdCfg {
+  static constexpr int kAtoms = (D + 63) / 64;
+  static constexpr int kStatBytes = kAtoms * BR * 128;  // one stationary operand
+  static constexpr int kMvBytes = kAtoms * BC * 128;    // one moving operand, one stage
+  static constexpr int kNS = MODE == kKV ? 2 : 3;        // moving stages
+  static constexpr int kOpRowBytes = BR * 128;          // one P / dS operand buffer
+  static constexpr int kNOps = MODE == kKV ? 2 : 1;      // P^T and dS^T, or dS
+  static constexpr int kStageLse = 4 * 2 * BC * 4;       // per-warp lse / delta staging (kKV)
+  static constexpr int kSmemBytes = 2 * kStatBytes + kNS * 2 * kMvBytes +
+                                    2 * kNOps * kOpRowBytes + kStageLse + 512 + 1024;
+  static constexpr int kTmemCols = 512;
+  // Score buffers: S at buf * 128, dP at buf * 128 + 64; accumulators after.
+  __host__ __device__ static constexpr int s_col(int buf) { return buf * 128; }
+  __host__ __device__ static constexpr int dp_col(int buf) { return buf * 128 + 64; }
+  __host__ __device__ static constexpr int acc_col(int i) { return 256 + i * D; }
+};
+
+struct BwdParams {
+  CUtensorMap t_stat0, t_stat1, t_mv0, t_mv1;  // 4-D maps {d, dim1, dim2, batch}
+  SwaBwdArgs a;
+  int seq_dim;
+  int num_items, blocks;
+};
+
+__device__ __forceinline__ void tma_rows(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                         int h, int t, int b, int seq_dim) {
+  if (seq_dim == 2)
+    tma_load_4d(dst, map, bar, x, h, t, b);
+  else
+    tma_load_4d(dst, map, bar, x, t, h, b);
+}
+
+struct Item {
+  int r0, h, b, t_lo, n_tiles;  // stationary rows r0 .. r0+127; moving tiles t_lo ..
+};
+
+// kKV: key blocks in increasing order (most query tiles first); kQ: query
+// blocks in decreasing order (most key tiles first).
+template <int MODE>
+__device__ __forceinline__ Item decode_item(const BwdParams& P, int item) {
+  Item it;
+  const int per_block = P.a.heads * P.a.batch;
+  const int blk = MODE == kKV ? item / per_block : P.blocks - 1 - item / per_block;
+  const int rest = item % per_block;
+  it.h = rest % P.a.heads;
+  it.b = rest / P.a.heads;
+  it.r0 = blk * BR;
+  int lo, hi;
+  if (MODE == kKV) {  // queries that see any of keys r0 .. r0+127
+    lo = it.r0;
+    hi = min(P.a.seq - 1, it.r0 + BR - 1 + P.a.window - 1);
+  } else {            // keys seen by any of queries r0 .. r0+127
+    lo = max(0, it.r0 - P.a.window + 1);
+    hi = min(P.a.seq - 1, it.r0 + BR - 1);
+  }
+  it.t_lo = lo / BC;
+  it.n_tiles = hi / BC - it.t_lo + 1;
+  return it;
+}
+
+// D columns of one TMEM lane row (fp32) into v.
+template <int D>
+__device__ __forceinline__ void tmem_row(uint32_t taddr, float (&v)[D]) {
+  if constexpr (D % 32 == 0) {
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(taddr + c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[c + e] = __uint_as_float(r[e]);
+    }
+  } else {
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(taddr, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float (&v)[D], float mul) {
+#pragma unroll
+  for (int e = 0; e < D; e += 8)
+    *reinterpret_cast<uint4*>(dst + e) =
+        make_uint4(pack_bf16x2(v[e] * mul, v[e + 1] * mul), pack_bf16x2(v[e + 2] * mul, v[e + 3] * mul),
+                   pack_bf16x2(v[e + 4] * mul, v[e + 5] * mul),
+                   pack_bf16x2(v[e + 6] * mul, v[e + 7] * mul));
+}
+
+// One 64-value bf16 operand row (128 bytes) into row r of a 128-byte-swizzled
+// K-major tile: 16-byte chunk c sits at chunk position c ^ (r % 8).
+__device__ __forceinline__ void store_op_row(uint8_t* tile, int r, const uint32_t (&pk)[32]) {
+  uint8_t* row = tile + r * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
+        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+}
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_constant__ BwdParams P) {
+  using C = BwdCfg<D, MODE>;
+  constexpr int NS = C::kNS;
+  const SwaBwdArgs& a = P.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sStat = smem;                               // [2][kStatBytes]
+  uint8_t* sMv = sStat + 2 * C::kStatBytes;            // [NS][2][kMvBytes]
+  uint8_t* sOp = sMv + NS * 2 * C::kMvBytes;           // [2 buffers][kNOps][kOpRowBytes]
+  float* sLse = reinterpret_cast<float*>(sOp + 2 * C::kNOps * C::kOpRowBytes);  // [4][2][BC]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sLse) + C::kStageLse);
+  uint64_t* stat_full = bars;
+  uint64_t* stat_empty = stat_full + 1;
+  uint64_t* mv_full = stat_empty + 1;   // [NS]
+  uint64_t* mv_empty = mv_full + NS;    // [NS]
+  uint64_t* s_full = mv_empty + NS;     // [2]
+  uint64_t* p_full = s_full + 2;        // [2]
+  uint64_t* op_done = p_full + 2;       // [2]
+  uint64_t* acc_full = op_done + 2;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* done_bar = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(stat_full, 1);
+    mbar_init(stat_empty, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&mv_full[s], 1);
+      mbar_init(&mv_empty[s], 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&s_full[k], 1);
+      mbar_init(&p_full[k], 4);
+      mbar_init(&op_done[k], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&P.t_stat0);
+    tma_prefetch_desc(&P.t_stat1);
+    tma_prefetch_desc(&P.t_mv0);
+    tma_prefetch_desc(&P.t_mv1);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- TMA --
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t mv_count = 0, stat_count = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
+        const Item it = decode_item<MODE>(P, item);
+        if (!mbar_wait(stat_empty, (stat_count & 1) ^ 1u, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(stat_full, 2 * C::kStatBytes);
+#pragma unroll
+        for (int at = 0; at < C::kAtoms; ++at) {
+          tma_rows(sStat + at * BR * 128, &P.t_stat0, stat_full, at * 64, it.h, it.r0, it.b,
+                   P.seq_dim);
+          tma_rows(sStat + C::kStatBytes + at * BR * 128, &P.t_stat1, stat_full, at * 64, it.h,
+                   it.r0, it.b, P.seq_dim);
+        }
+        ++stat_count;
+        for (int j = 0; j < it.n_tiles; ++j, ++mv_count) {
+          const int st = mv_count % NS;
+          const uint32_t ph = (mv_count / NS) & 1;
+          if (!mbar_wait(&mv_empty[st], ph ^ 1u, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          const int row0 = (it.t_lo + j) * BC;
+          uint8_t* dst = sMv + st * 2 * C::kMvBytes;
+          mbar_arrive_expect_tx(&mv_full[st], 2 * C::kMvBytes);
+#pragma unroll
+          for (int at = 0; at < C::kAtoms; ++at) {
+            tma_rows(dst + at * BC * 128, &P.t_mv0, &mv_full[st], at * 64, it.h, row0, it.b,
+                     P.seq_dim);
+            tma_rows(dst + C::kMvBytes + at * BC * 128, &P.t_mv1, &mv_full[st], at * 64, it.h,
+                     row0, it.b, P.seq_dim);
+          }
+          armed |= 1u << st;
+          armed_parity = (armed_parity & ~(1u << st)) | (ph << st);
+        }
+      }
+      // Let every copy this thread issued land before the CTA goes away.
+      volatile int no_abort = 0;
+      for (int s = 0; s < NS; ++s)
+        if (armed & (1u << s))
+          mbar_wait(&mv_full[s], (armed_parity >> s) & 1u, &no_abort, a.status);
+      if (stat_count > 0) mbar_wait(stat_full, (stat_count - 1) & 1, &no_abort, a.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA --
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = umma_idesc_bf16(BR, BC);
+      constexpr uint32_t idesc_acc = umma_idesc_bf16(BR, D) | (1u << 16);  // B MN-major
+      bool ok = true;
+      uint32_t mv_count = 0, stat_count = 0, s_issued = 0, op_issued = 0, items_done = 0;
+      const uint32_t stat0 = smem_addr(sStat), stat1 = stat0 + C::kStatBytes;
+      for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
+        const Item it = decode_item<MODE>(P, item);
+        if (!mbar_wait(stat_full, stat_count & 1, abort_flag, a.status)) break;
+        ++stat_count;
+        tc_fence_after();
+        for (int j = 0; ok && j <= it.n_tiles; ++j) {
+          if (j < it.n_tiles) {
+            const uint32_t mc = mv_count + j;
+            const int st = mc % NS;
+            if (!mbar_wait(&mv_full[st], (mc / NS) & 1, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t mv0 = smem_addr(sMv + st * 2 * C::kMvBytes), mv1 = mv0 + C::kMvBytes;
+            const int buf = s_issued & 1;
+            // Scores of stationary rows against the moving tile:
+            //   kKV: S^T = K Q^T, dP^T = V dO^T;  kQ: S = Q K^T, dP = dO V^T.
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t at = kk / 4, off = (kk % 4) * 32;
+              umma_bf16_ss(tmem + C::s_col(buf), sw128_kmajor_desc(stat0 + at * BR * 128 + off),
+                           sw128_kmajor_desc(mv0 + at * BC * 128 + off), idesc_s, kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t at = kk / 4, off = (kk % 4) * 32;
+              umma_bf16_ss(tmem + C::dp_col(buf), sw128_kmajor_desc(stat1 + at * BR * 128 + off),
+                           sw128_kmajor_desc(mv1 + at * BC * 128 + off), idesc_s, kk > 0);
+            }
+            umma_commit(&s_full[buf]);
+            ++s_issued;
+            if (j == it.n_tiles - 1) umma_commit(stat_empty);  // stationary tiles are free
+          }
+          if (j >= 1) {
+            const uint32_t mc = mv_count + j - 1;
+            const int st = mc % NS;
+            const uint32_t mv0 = smem_addr(sMv + st * 2 * C::kMvBytes), mv1 = mv0 + C::kMvBytes;
+            const uint32_t n = op_issued;  // operand buffer n % 2
+            if (!mbar_wait(&p_full[n & 1], (n >> 1) & 1, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            if (j == 1) {  // the accumulators of the previous item have been read out
+              if (!mbar_wait(acc_empty, (items_done & 1) ^ 1u, abort_flag, a.status)) {
+                ok = false;
+                break;
+              }
+            }
+            tc_fence_after();
+            const uint32_t op = smem_addr(sOp + (n & 1) * C::kNOps * C::kOpRowBytes);
+            const bool first = j == 1;
+            // The moving tile as the MN-major B operand: rows = its 64
+            // positions (K), 64-column blocks of d (N) 64 * 128 bytes apart.
+            if constexpr (MODE == kKV) {
+              // dV += P^T dO, dK += dS^T Q
+#pragma unroll
+              for (int kk = 0; kk < BC / 16; ++kk)
+                umma_bf16_ss(tmem + C::acc_col(0), sw128_kmajor_desc(op + kk * 32),
+                             sw128_mnmajor_desc(mv1 + kk * 16 * 128, BC * 128), idesc_acc,
+                             (!first || kk > 0) ? 1u : 0u);
+#pragma unroll
+              for (int kk = 0; kk < BC / 16; ++kk)
+                umma_bf16_ss(tmem + C::acc_col(1), sw128_kmajor_desc(op + C::kOpRowBytes + kk * 32),
+                             sw128_mnmajor_desc(mv0 + kk * 16 * 128, BC * 128), idesc_acc,
+                             (!first || kk > 0) ? 1u : 0u);
+            } else {
+              // dQ += dS K
+#pragma unroll
+              for (int kk = 0; kk < BC / 16; ++kk)
+                umma_bf16_ss(tmem + C::acc_col(0), sw128_kmajor_desc(op + kk * 32),
+                             sw128_mnmajor_desc(mv0 + kk * 16 * 128, BC * 128), idesc_acc,
+                             (!first || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(&op_done[n & 1]);
+            umma_commit(&mv_empty[st]);
+            ++op_issued;
+          }
+        }
+        if (!ok) break;
+        umma_commit(acc_full);
+        ++items_done;
+        mv_count += it.n_tiles;
+      }
+      umma_commit(done_bar);
+      volatile int no_abort = 0;
+      mbar_wait(done_bar, 0, &no_abort, a.status);
+    }
+  } else {
+    // ------------------------------------------------- P, dS and output --
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // stationary row = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    float* wl = sLse + (warp - 2) * 2 * BC;  // this warp's lse / delta staging (kKV)
+    uint32_t seen = 0, items_done = 0;
+    bool ok = true;
+    auto wait_op = [&](uint32_t n) -> bool {  // operand buffer n % 2 free again
+      if (!mbar_wait_warp(&op_done[n & 1], (n >> 1) & 1, abort_flag, a.status)) return false;
+      tc_fence_after();
+      return true;
+    };
+    for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
+      const Item it = decode_item<MODE>(P, item);
+      const int row = it.r0 + r;  // this thread's stationary position
+      const int64_t bh = static_cast<int64_t>(it.b) * a.heads + it.h;
+      float lse_row = 0.f, delta_row = 0.f;
+      if (MODE == kQ && row < a.seq) {
+        lse_row = a.lse[bh * a.seq + row];
+        delta_row = a.delta[bh * a.seq + row];
+      }
+      for (int t = 0; t < it.n_tiles; ++t) {
+        const int c0 = (it.t_lo + t) * BC;  // first moving position of the tile
+        const int buf = seen & 1;
+        if (MODE == kKV) {  // per-query lse and delta of the tile, staged per warp
+          __syncwarp();
+          for (int e = lane; e < BC; e += 32) {
+            const int q = c0 + e;
+            wl[e] = q < a.seq ? a.lse[bh * a.seq + q] : 0.f;
+            wl[BC + e] = q < a.seq ? a.delta[bh * a.seq + q] : 0.f;
+          }
+          __syncwarp();
+        }
+        if (!mbar_wait_warp(&s_full[buf], (seen >> 1) & 1, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float s[BC], dp[BC];
+#pragma unroll
+        for (int c = 0; c < BC; c += 32) {
+          uint32_t raw[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + C::s_col(buf) + c, raw);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[c + e] = __uint_as_float(raw[e]);
+          tmem_ld_32x32b_x32(tmem + lane_base + C::dp_col(buf) + c, raw);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) dp[c + e] = __uint_as_float(raw[e]);
+        }
+        uint32_t pk_p[BC / 2], pk_ds[BC / 2];
+#pragma unroll
+        for (int e = 0; e < BC; e += 2) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = c0 + e + u;  // moving position
+            // kKV: key `row`, query c;  kQ: query `row`, key c.
+            const int qi = MODE == kKV ? c : row;
+            const int kj = MODE == kKV ? row : c;
+            const bool vis = kj <= qi && qi - kj < a.window && qi < a.seq && kj < a.seq;
+            const float l2 = MODE == kKV ? wl[e + u] : lse_row;
+            const float dl = MODE == kKV ? wl[BC + e + u] : delta_row;
+            const float p = vis ? fast_exp2(s[e + u] * a.scale_log2 - l2) : 0.f;
+            pv[u] = p;
+            dsv[u] = p * (dp[e + u] - dl);
+          }
+          pk_p[e / 2] = pack_bf16x2(pv[0], pv[1]);
+          pk_ds[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        // Operand buffer `buf` was last read by the accumulate MMAs seen - 2.
+        if (seen >= 2 && !wait_op(seen - 2)) {
+          ok = false;
+          break;
+        }
+        uint8_t* ops = sOp + buf * C::kNOps * C::kOpRowBytes;
+        if constexpr (MODE == kKV) {
+          store_op_row(ops, r, pk_p);
+          store_op_row(ops + C::kOpRowBytes, r, pk_ds);
+        } else {
+          store_op_row(ops, r, pk_ds);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[buf]);
+        ++seen;
+      }
+      if (!ok) break;
+      // All accumulate MMAs of the item are done: gradients out.
+      if (!mbar_wait_warp(acc_full, items_done & 1, abort_flag, a.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int prow = row < a.seq ? row : 0;
+      float g[D];
+      if constexpr (MODE == kKV) {
+        tmem_row<D>(tmem + lane_base + C::acc_col(0), g);
+        if (row < a.seq) store_row_bf16<D>(a.dv + it.b * a.dv_sb + it.h * a.dv_sh + prow * a.dv_ss, g, 1.f);
+        tmem_row<D>(tmem + lane_base + C::acc_col(1), g);
+        if (row < a.seq)
+          store_row_bf16<D>(a.dk + it.b * a.dk_sb + it.h * a.dk_sh + prow * a.dk_ss, g, a.scale);
+      } else {
+        tmem_row<D>(tmem + lane_base + C::acc_col(0), g);
+        if (row < a.seq)
+          store_row_bf16<D>(a.dq + it.b * a.dq_sb + it.h * a.dq_sh + prow * a.dq_ss, g, a.scale);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      ++items_done;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// delta_i = sum_c dO_ic * o_ic for every (batch entry, head, row): one
+// thread per row, 16-byte loads.
+__global__ void swa_delta_kernel(const SwaBwdArgs a) {
+  const int64_t rows = static_cast<int64_t>(a.batch) * a.heads * a.seq;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < rows;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(idx % a.seq);
+    const int64_t bh = idx / a.seq;
+    const int h = static_cast<int>(bh % a.heads);
+    const int b = static_cast<int>(bh / a.heads);
+    const uint4* o = reinterpret_cast<const uint4*>(a.o + b * a.o_sb + h * a.o_sh + i * a.o_ss);
+    const uint4* g = reinterpret_cast<const uint4*>(a.dout + b * a.do_sb + h * a.do_sh +
+                                                    i * a.do_ss);
+    float acc = 0.f;
+    for (int v = 0; v < a.head_dim / 8; ++v) {
+      const uint4 x = __ldg(o + v), y = __ldg(g + v);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        acc += bf16_lo(xs[e]) * bf16_lo(ys[e]) + bf16_hi(xs[e]) * bf16_hi(ys[e]);
+    }
+    a.delta[idx] = acc;
+  }
+}
+
+template <int D, int MODE>
+cudaError_t launch_typed(const BwdParams& prm, int grid, cudaStream_t stream) {
+  using C = BwdCfg<D, MODE>;
+  static_assert(C::kSmemBytes <= 227 * 1024, "shared memory");
+  auto kern = swa_bwd_kernel<D, MODE>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t dispatch(const BwdParams& prm, int grid, cudaStream_t stream) {
+  switch (prm.a.head_dim) {
+    case 16: return launch_typed<16, MODE>(prm, grid, stream);
+    case 32: return launch_typed<32, MODE>(prm, grid, stream);
+    case 64: return launch_typed<64, MODE>(prm, grid, stream);
+    case 96: return launch_typed<96, MODE>(prm, grid, stream);
+    case 128: return launch_typed<128, MODE>(prm, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// 4-D map {d, heads, seq, batch} or {d, seq, heads, batch} over a strided
+// [batch][heads][seq][d] view; boxes of 64 columns x `rows` positions.
+bool bwd_map(CUtensorMap* map, const __nv_bfloat16* base, int64_t sb, int64_t sh, int64_t ss,
+             const SwaBwdArgs& a, int rows, int* seq_dim) {
+  const bool heads_first = sh <= ss;
+  if (sb <= 0) sb = (sh > ss ? sh : ss) * (a.heads > a.seq ? a.heads : a.seq);  // unused stride
+  const uint64_t dims[4] = {static_cast<uint64_t>(a.head_dim),
+                            static_cast<uint64_t>(heads_first ? a.heads : a.seq),
+                            static_cast<uint64_t>(heads_first ? a.seq : a.heads),
+                            static_cast<uint64_t>(a.batch)};
+  const uint64_t strides[3] = {static_cast<uint64_t>(heads_first ? sh : ss) * 2,
+                               static_cast<uint64_t>(heads_first ? ss : sh) * 2,
+                               static_cast<uint64_t>(sb) * 2};
+  const uint32_t box[4] = {64, heads_first ? 1u : static_cast<uint32_t>(rows),
+                           heads_first ? static_cast<uint32_t>(rows) : 1u, 1};
+  *seq_dim = heads_first ? 2 : 1;
+  return make_tensor_map(map, base, 4, dims, strides, box);
+}
+
+}  // namespace
+
+cudaError_t launch_swa_backward(const SwaBwdArgs& a, cudaStream_t stream) {
+  if (a.seq <= 0 || a.batch <= 0 || a.heads <= 0) return cudaSuccess;
+  const int64_t rows = static_cast<int64_t>(a.batch) * a.heads * a.seq;
+  {
+    const int64_t blocks = (rows + 255) / 256;
+    const int grid = static_cast<int>(blocks < 8 * a.sms ? blocks : 8 * a.sms);
+    swa_delta_kernel<<<grid, 256, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  BwdParams prm;
+  prm.a = a;
+  prm.blocks = (a.seq + BR - 1) / BR;
+  const int64_t items = static_cast<int64_t>(prm.blocks) * a.heads * a.batch;
+  if (items > 0x7fffffff) return cudaErrorInvalidValue;
+  prm.num_items = static_cast<int>(items);
+  const int grid = static_cast<int>(items < a.sms ? items : a.sms);
+  int sd[4];
+  // dK, dV: stationary K, V (128 rows); moving Q, dO (64 rows).
+  if (!bwd_map(&prm.t_stat0, a.k, a.k_sb, a.k_sh, a.k_ss, a, BR, &sd[0]) ||
+      !bwd_map(&prm.t_stat1, a.v, a.v_sb, a.v_sh, a.v_ss, a, BR, &sd[1]) ||
+      !bwd_map(&prm.t_mv0, a.q, a.q_sb, a.q_sh, a.q_ss, a, BC, &sd[2]) ||
+      !bwd_map(&prm.t_mv1, a.dout, a.do_sb, a.do_sh, a.do_ss, a, BC, &sd[3]))
+    return cudaErrorInvalidValue;
+  if (sd[0] != sd[1] || sd[0] != sd[2] || sd[0] != sd[3]) return cudaErrorInvalidValue;
+  prm.seq_dim = sd[0];
+  cudaError_t e = dispatch<kKV>(prm, grid, stream);
+  if (e != cudaSuccess) return e;
+  // dQ: stationary Q, dO (128 rows); moving K, V (64 rows).
+  if (!bwd_map(&prm.t_stat0, a.q, a.q_sb, a.q_sh, a.q_ss, a, BR, &sd[0]) ||
+      !bwd_map(&prm.t_stat1, a.dout, a.do_sb, a.do_sh, a.do_ss, a, BR, &sd[1]) ||
+      !bwd_map(&prm.t_mv0, a.k, a.k_sb, a.k_sh, a.k_ss, a, BC, &sd[2]) ||
+      !bwd_map(&prm.t_mv1, a.v, a.v_sb, a.v_sh, a.v_ss, a, BC, &sd[3]))
+    return cudaErrorInvalidValue;
+  return dispatch<kQ>(prm, grid, stream);
+}
+
+}  // namespace ptb

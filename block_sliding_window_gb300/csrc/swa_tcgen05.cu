@@ -452,6 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
       tc_fence_before();
       if (COUNTS && i < a.seq)
         a.counts[(static_cast<int64_t>(it.b) * a.heads + it.h) * a.seq + i] = cnt;
+      // Every row attends to itself, so l_run > 0 and m_ref is finite here.
+      if (a.lse && i < a.seq)
+        a.lse[(static_cast<int64_t>(it.b) * a.heads + it.h) * a.seq + i] = m_ref + log2f(l_run);
     }
   }
 

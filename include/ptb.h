@@ -214,6 +214,57 @@ ptb_status ptb_forward_fp8_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
                                   ptb_bf16* y, void* workspace, size_t workspace_bytes,
                                   ptb_stream stream, void* const* events, int32_t n_events);
 
+/*
+ * Training: forward pass that keeps its activations, and the backward pass.
+ *
+ * The pages' workload is training: MegaScale counts 6N FLOPs per token, 2N
+ * forward and 4N backward (MegaScale study notes, ch.2 §2.1, MFU
+ * definition).  The backward pass is the chain rule of the PTB definition
+ * (§2.2, PTB row):
+ *   dW_o = dy^T ctx,   dW_down = dy^T G,   dctx = dy W_o,   dG = dy W_down,
+ *   dZ = dG * gelu_tanh'(Z),   [dQ | dK | dV] = SWA backward of dctx,
+ *   dxn = [dQ | dK | dV] W_qkv + dZ W_up,   [dW_qkv ; dW_up] = [dQ | dK | dV | dZ]^T xn,
+ *   dx = dy + LN backward of dxn,   dgamma, dbeta = sums over tokens.
+ *
+ * ptb_forward_train computes y exactly as ptb_forward does and writes into
+ * `saved` (caller-owned device memory of ptb_train_saved_size bytes, 256-byte
+ * aligned) what the backward pass reads: xn = LN(x), the per-token LN mean
+ * and 1/sqrt(var + eps) (fp32 pairs), U = [Q | K | V | G], the
+ * pre-activation Z = xn W_up^T, ctx, and the attention's per-row
+ * log-sum-exp (fp32, base 2).  `workspace` as in ptb_forward (null: the
+ * library arena).
+ *
+ * ptb_backward takes the upstream gradient dy [batch, seq, H] (bf16), the
+ * forward inputs x, ln_gamma and the four weights, and `saved` from
+ * ptb_forward_train on the same inputs; it writes dx (bf16, [batch, seq, H])
+ * and, in fp32, dln_gamma [H], dln_beta [H], dw_qkv [3H, H], dw_o [H, H],
+ * dw_up [F, H], dw_down [H, F] (same layouts as the weights; overwritten, not
+ * accumulated).  Scratch: `workspace` of ptb_backward_workspace_size bytes
+ * (256-byte aligned), or null for the library arena.  Ten kernels on
+ * `stream`: two GEMMs, the attention backward (three kernels), two GEMMs,
+ * the LayerNorm backward (three kernels), plus a counter reset before each
+ * GEMM whose last wave is split along K.  Sums run in a fixed order, so the
+ * results are the same bits on every call.  Shape rules, alignment and errors as in
+ * ptb_forward; PTB_ERR_WORKSPACE if `saved` is too small.
+ */
+size_t ptb_train_saved_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,
+                            int32_t heads);
+ptb_status ptb_forward_train(const ptb_bf16* x, const ptb_bf16* ln_gamma, const ptb_bf16* ln_beta,
+                             const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
+                             const ptb_bf16* w_down, int64_t batch, int64_t seq, int64_t hidden,
+                             int64_t ffn, int32_t heads, int32_t window, ptb_bf16* y, void* saved,
+                             size_t saved_bytes, void* workspace, size_t workspace_bytes,
+                             ptb_stream stream);
+size_t ptb_backward_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,
+                                   int32_t heads);
+ptb_status ptb_backward(const ptb_bf16* dy, const ptb_bf16* x, const ptb_bf16* ln_gamma,
+                        const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
+                        const ptb_bf16* w_down, const void* saved, size_t saved_bytes,
+                        int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
+                        int32_t window, ptb_bf16* dx, float* dln_gamma, float* dln_beta,
+                        float* dw_qkv, float* dw_o, float* dw_up, float* dw_down, void* workspace,
+                        size_t workspace_bytes, ptb_stream stream);
+
 /* Frees the library's own workspace arena on the current device (if any). */
 ptb_status ptb_release_workspace(void);
 
@@ -244,6 +295,32 @@ ptb_status swa_attention_strided(const ptb_bf16* q, int64_t q_sb, int64_t q_sh, 
                                  ptb_bf16* o, int64_t o_sb, int64_t o_sh, int64_t o_ss,
                                  int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
                                  int32_t window, float scale, ptb_stream stream);
+
+/*
+ * swa_attention_lse: swa_attention that also writes, for every row
+ * (b, h, i), lse[(b*heads + h)*seq + i] = log2(sum_j 2^(q_i.k_j * scale *
+ * log2 e)) over the row's window (fp32, device memory): the softmax
+ * denominator in base 2, which swa_attention_backward needs.
+ *
+ * swa_attention_backward: gradients of o = SWA(q, k, v) (contiguous
+ * [batch, heads, seq, head_dim] bf16, as swa_attention) for the upstream
+ * gradient dout, given o and lse from swa_attention_lse with the same scale:
+ *   dv = P^T dout,  dP = dout v^T,  dS = P * (dP - rowsum(dout * o)),
+ *   dq = scale * dS k,  dk = scale * dS^T q,
+ * P recomputed from q, k and lse.  dq, dk, dv are bf16 of the same shape;
+ * delta is fp32 scratch of batch*heads*seq elements.  Four launches
+ * (rowsum, dK/dV over 128-key blocks, dQ over 128-query blocks), no atomics.
+ * Shape and alignment rules as swa_attention.
+ */
+ptb_status swa_attention_lse(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v,
+                             int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
+                             int32_t window, float scale, ptb_bf16* o, float* lse,
+                             ptb_stream stream);
+ptb_status swa_attention_backward(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v,
+                                  const ptb_bf16* o, const ptb_bf16* dout, const float* lse,
+                                  int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
+                                  int32_t window, float scale, ptb_bf16* dq, ptb_bf16* dk,
+                                  ptb_bf16* dv, float* delta, ptb_stream stream);
 
 /*
  * swa_attention_counts: runs the attention kernel's own masking code and
