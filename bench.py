@@ -38,7 +38,9 @@ METRIC = "PTB-layer fwd tokens/s and TFLOP/s (bf16) on 1 GB300; % of tensor peak
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 GEMM_SRC = os.path.join(ROOT, "block_sliding_window_gb300", "csrc", "gemm_tcgen05.cu")
-SWA_SRC = os.path.join(ROOT, "block_sliding_window_gb300", "csrc", "swa.cu")
+SWA_SRC = os.path.join(ROOT, "block_sliding_window_gb300", "csrc", "swa_tcgen05.cu")
+TRAIN_METRIC = ("PTB-layer training step (forward + backward) tokens/s and TFLOP/s (bf16) on "
+                "1 GB300; % of tensor peak")
 
 
 def layer_flops(cfg) -> dict:
@@ -52,6 +54,17 @@ def layer_flops(cfg) -> dict:
             "band_keys": band * cfg.batch * cfg.heads}
 
 
+def backward_flops(cfg) -> dict:
+    """Algorithmic backward FLOPs: an input-gradient and a weight-gradient
+    GEMM per forward GEMM, and dV, dP, dQ, dK over the in-band pairs."""
+    fl = layer_flops(cfg)
+    band = fl["band_keys"] // cfg.heads
+    attn = 8 * cfg.hidden * band
+    gemm = 2 * (fl["gemm1"] + fl["gemm2"])
+    return {"dgrad_out": fl["gemm2"], "wgrad_out": fl["gemm2"], "dgrad_in": fl["gemm1"],
+            "wgrad_in": fl["gemm1"], "attn": attn, "total": gemm + attn}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -62,9 +75,12 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def sha_of(path: str) -> str:
-    with open(path, "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()[:16]
+def sha_of(path: str):
+    try:
+        with open(path, "rb") as fh:
+            return hashlib.sha256(fh.read()).hexdigest()[:16]
+    except OSError:
+        return None
 
 
 def traffic_for(kernel: str, workload: str, src: str):
@@ -307,6 +323,131 @@ def run_swa(args, world, rank, local):
             "clocks": clk, "gpu_launches": args.steps}), flush=True)
 
 
+def run_train(args, world, rank, local):
+    """One training step of the layer: ptb_forward_train + ptb_backward."""
+    import block_sliding_window_gb300 as bsw
+    cfg = workload_config(args.workload)
+    d = workloads.ptb_inputs(cfg, device="cuda")
+    dy = workloads.normal_bf16(tuple(d["x"].shape), seed=cfg.seed + 1000, device="cuda")
+    b, s, h, f = cfg.batch, cfg.seq, cfg.hidden, cfg.ffn
+    saved = torch.empty(bsw.train_saved_size(b, s, h, f, cfg.heads), dtype=torch.uint8,
+                        device="cuda")
+    ws_f = torch.empty(bsw.workspace_size(b, s, h, f), dtype=torch.uint8, device="cuda")
+    ws_b = torch.empty(bsw.backward_workspace_size(b, s, h, f, cfg.heads), dtype=torch.uint8,
+                       device="cuda")
+    y = torch.empty_like(d["x"])
+    dev, f32 = "cuda", torch.float32
+    grads = dict(dx=torch.empty_like(d["x"]), dln_gamma=torch.empty(h, dtype=f32, device=dev),
+                 dln_beta=torch.empty(h, dtype=f32, device=dev),
+                 dw_qkv=torch.empty(3 * h, h, dtype=f32, device=dev),
+                 dw_o=torch.empty(h, h, dtype=f32, device=dev),
+                 dw_up=torch.empty(f, h, dtype=f32, device=dev),
+                 dw_down=torch.empty(h, f, dtype=f32, device=dev))
+    w = (d["w_qkv"], d["w_o"], d["w_up"], d["w_down"])
+    stream = torch.cuda.current_stream()
+
+    def step(x_in, dy_in, marks=None):
+        if marks is not None:
+            marks[0].record(stream)
+        bsw.ptb_forward_train(x_in, d["ln_gamma"], d["ln_beta"], *w, cfg.heads, cfg.window, y=y,
+                              saved=saved, workspace=ws_f)
+        if marks is not None:
+            return bsw.ptb_backward_events(dy_in, x_in, d["ln_gamma"], *w, saved, cfg.heads,
+                                           cfg.window, marks[1:], grads=grads, workspace=ws_b)
+        return bsw.ptb_backward(dy_in, x_in, d["ln_gamma"], *w, saved, cfg.heads, cfg.window,
+                                grads=grads, workspace=ws_b)
+
+    for _ in range(args.warmup):
+        step(d["x"], dy)
+    torch.cuda.synchronize()
+    if bsw.last_device_error() != 0:
+        raise RuntimeError("device status set during warm-up")
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(d["x"], dy, marks[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    if bsw.last_device_error() != 0:
+        raise RuntimeError("device status set in the timed region")
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world)
+    names = ["forward_train", "dgrad_out", "wgrad_out", "swa_backward", "dgrad_in", "wgrad_in",
+             "layernorm_backward"]
+    per_kernel = {n: sum(m[j].elapsed_time(m[j + 1]) for m in marks) / args.steps
+                  for j, n in enumerate(names)}
+    per_step = [m[0].elapsed_time(m[-1]) for m in marks]
+
+    # End to end through the public calls: x and dy in from pinned host
+    # memory, dx out, every step (the weight gradients stay on the device
+    # for the optimizer).
+    x_host, dy_host = d["x"].cpu().pin_memory(), dy.cpu().pin_memory()
+    dx_host = torch.empty(d["x"].shape, dtype=torch.bfloat16, pin_memory=True)
+    x_dev, dy_dev = torch.empty_like(d["x"]), torch.empty_like(dy)
+    for _ in range(max(1, args.warmup)):
+        x_dev.copy_(x_host, non_blocking=True)
+        dy_dev.copy_(dy_host, non_blocking=True)
+        step(x_dev, dy_dev)
+        dx_host.copy_(grads["dx"], non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        dy_dev.copy_(dy_host, non_blocking=True)
+        step(x_dev, dy_dev)
+        dx_host.copy_(grads["dx"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+
+    fwd, bwd = layer_flops(cfg), backward_flops(cfg)
+    total = fwd["total"] + bwd["total"]
+    peaks, peak_src = load_peaks()
+    peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    tokens = cfg.tokens * world
+    tflops = total * world / (ms * 1e-3) / 1e12
+    # Dominant kernel: the slowest backward GEMM of the step.
+    gemms = ["dgrad_out", "wgrad_out", "dgrad_in", "wgrad_in"]
+    top = max(gemms, key=lambda n: per_kernel[n])
+    top_tf = bwd[top] / (per_kernel[top] * 1e-3) / 1e12
+    line = {
+        "metric": TRAIN_METRIC, "value": tokens / (ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_json(args.workload, cfg, world),
+        "tflops": tflops,
+        "pct_of_peak": {"burst": 100 * tflops / world / peaks["bf16_tflops"],
+                        "sustained": 100 * tflops / world / peak_sus, "source": peak_src},
+        "kernels_ms": per_kernel,
+        "step_ms": {"mean": sum(per_step) / len(per_step),
+                    "median": statistics.median(per_step), "min": min(per_step)},
+        "flops": {"forward": fwd["total"], "backward": bwd["total"]},
+        "roofline": {"bound": "tensor", "kernel": f"{top} (tcgen05 GEMM, backward)",
+                     "achieved": top_tf, "peak": peak_sus, "unit": "TFLOP/s",
+                     "frac": top_tf / peak_sus, "peak_source": f"{peak_src} bf16 sustained",
+                     "traffic": traffic_for(top, args.workload + "_train", GEMM_SRC),
+                     "algorithmic_flops_per_launch": bwd[top]},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * x_host.numel() * 2,
+                "d2h_bytes_per_step": dx_host.numel() * 2},
+        "clocks": clk,
+        "gpu_launches": 14 * args.steps,
+        "cpu_baseline": None,
+        "cpu_baseline_note": "the fp64 backward oracle has no row-sampled form; see --pass forward",
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_ours(args, world, rank, local):
     import block_sliding_window_gb300 as bsw
     from block_sliding_window_gb300 import build as _build
@@ -314,6 +455,8 @@ def run_ours(args, world, rank, local):
     bsw.load()
     if args.workload == "swa":
         return run_swa(args, world, rank, local)
+    if args.pass_ == "train":
+        return run_train(args, world, rank, local)
     cfg = workload_config(args.workload)
     d = workloads.ptb_inputs(cfg, device="cuda")
     serial = args.block == "serial"
@@ -476,6 +619,8 @@ def main():
                     help="the parallel block (default) or the serial block it replaces")
     ap.add_argument("--precision", choices=["bf16", "fp8"], default="bf16",
                     help="bf16 (default) or the variant with e4m3 GEMM operands")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "train"], default="forward",
+                    help="the layer forward (default) or a training step (forward + backward)")
     ap.add_argument("--cpu-rows", type=int, default=1024,
                     help="rows of the layer the CPU baseline computes (about 10 s of oracle work)")
     ap.add_argument("--ref-rows", type=int, default=64,

@@ -22,7 +22,7 @@ __all__ = [
     "gemm_out_down", "gemm_workspace_size", "workspace_size", "release_workspace", "last_device_error",
     "wait_probe", "serial_forward", "serial_workspace_size", "prepare_fp8_weights",
     "fp8_workspace_size", "ptb_forward_fp8", "ptb_forward_fp8_events", "train_saved_size",
-    "ptb_forward_train", "backward_workspace_size", "ptb_backward", "swa_attention_lse",
+    "ptb_forward_train", "backward_workspace_size", "ptb_backward", "ptb_backward_events", "swa_attention_lse",
     "swa_attention_backward", "LIB_PATH", "SYMBOLS",
 ]
 
@@ -52,6 +52,8 @@ SYMBOLS = {
     "ptb_forward_train": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p, _sz, _p]),
     "ptb_backward_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i32]),
     "ptb_backward": (_st, [_p] * 8 + [_sz] + [_i64] * 4 + [_i32, _i32] + [_p] * 8 + [_sz, _p]),
+    "ptb_backward_events": (_st, [_p] * 8 + [_sz] + [_i64] * 4 + [_i32, _i32] + [_p] * 8
+                            + [_sz, _p, _p, _i32]),
     "swa_attention_lse": (_st, [_p, _p, _p, _i64, _i32, _i64, _i32, _i32, ctypes.c_float, _p, _p,
                                 _p]),
     "swa_attention_backward": (_st, [_p] * 6 + [_i64, _i32, _i64, _i32, _i32, ctypes.c_float]
@@ -354,6 +356,20 @@ def ptb_backward(dy, x, ln_gamma, w_qkv, w_o, w_up, w_down, saved, heads: int, w
     """Gradients of the layer for upstream dy: dx (bf16) and fp32 dln_gamma,
     dln_beta, dw_qkv, dw_o, dw_up, dw_down, returned as a dict (or written
     into `grads`, a dict of preallocated tensors with those keys)."""
+    return _backward(dy, x, ln_gamma, w_qkv, w_o, w_up, w_down, saved, heads, window, grads,
+                     workspace, stream, None)
+
+
+def ptb_backward_events(dy, x, ln_gamma, w_qkv, w_o, w_up, w_down, saved, heads: int,
+                        window: int, events, grads=None, workspace=None, stream=None) -> dict:
+    """ptb_backward that also records 7 torch.cuda.Event objects at its
+    kernel boundaries (see the C declaration)."""
+    return _backward(dy, x, ln_gamma, w_qkv, w_o, w_up, w_down, saved, heads, window, grads,
+                     workspace, stream, events)
+
+
+def _backward(dy, x, ln_gamma, w_qkv, w_o, w_up, w_down, saved, heads, window, grads, workspace,
+              stream, events):
     lib = load()
     (batch, seq, hidden, ffn), _, ws_bytes = _ptb_args(
         x, ln_gamma, ln_gamma, w_qkv, w_o, w_up, w_down, heads, window, dy, workspace)
@@ -369,12 +385,21 @@ def ptb_backward(dy, x, ln_gamma, w_qkv, w_o, w_up, w_down, saved, heads: int, w
                      dw_up=torch.empty(ffn, hidden, dtype=f32, device=dev),
                      dw_down=torch.empty(hidden, ffn, dtype=f32, device=dev))
     g = grads
-    st = lib.ptb_backward(_ptr(dy), _ptr(x), _ptr(ln_gamma), _ptr(w_qkv), _ptr(w_o), _ptr(w_up),
-                          _ptr(w_down), _ptr(saved), saved.numel(), batch, seq, hidden, ffn, heads,
-                          window, _ptr(g["dx"]), _ptr(g["dln_gamma"]), _ptr(g["dln_beta"]),
-                          _ptr(g["dw_qkv"]), _ptr(g["dw_o"]), _ptr(g["dw_up"]),
-                          _ptr(g["dw_down"]), _ptr(workspace), ws_bytes, _stream(stream))
-    _check(st, "ptb_backward")
+    args = (_ptr(dy), _ptr(x), _ptr(ln_gamma), _ptr(w_qkv), _ptr(w_o), _ptr(w_up), _ptr(w_down),
+            _ptr(saved), saved.numel(), batch, seq, hidden, ffn, heads, window, _ptr(g["dx"]),
+            _ptr(g["dln_gamma"]), _ptr(g["dln_beta"]), _ptr(g["dw_qkv"]), _ptr(g["dw_o"]),
+            _ptr(g["dw_up"]), _ptr(g["dw_down"]), _ptr(workspace), ws_bytes, _stream(stream))
+    if events is None:
+        _check(lib.ptb_backward(*args), "ptb_backward")
+        return g
+    if len(events) != 7:
+        raise ValueError("need 7 events")
+    st_obj = torch.cuda.current_stream() if stream is None else stream
+    for ev in events:
+        if not ev.cuda_event:  # torch creates the CUDA event on its first record
+            ev.record(st_obj)
+    handles = (ctypes.c_void_p * 7)(*[ev.cuda_event for ev in events])
+    _check(lib.ptb_backward_events(*args, handles, 7), "ptb_backward_events")
     return g
 
 

@@ -1158,18 +1158,29 @@ size_t ptb_backward_workspace_size(int64_t batch, int64_t seq, int64_t hidden, i
   return bwd_layout(batch, seq, hidden, ffn, heads, current_sms()).total;
 }
 
-ptb_status ptb_backward(const ptb_bf16* dy, const ptb_bf16* x, const ptb_bf16* ln_gamma,
-                        const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
-                        const ptb_bf16* w_down, const void* saved, size_t saved_bytes,
-                        int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
-                        int32_t window, ptb_bf16* dx, float* dln_gamma, float* dln_beta,
-                        float* dw_qkv, float* dw_o, float* dw_up, float* dw_down, void* workspace,
-                        size_t workspace_bytes, ptb_stream stream_) {
+ptb_status ptb_backward_events(const ptb_bf16* dy, const ptb_bf16* x, const ptb_bf16* ln_gamma,
+                               const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
+                               const ptb_bf16* w_down, const void* saved, size_t saved_bytes,
+                               int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,
+                               int32_t heads, int32_t window, ptb_bf16* dx, float* dln_gamma,
+                               float* dln_beta, float* dw_qkv, float* dw_o, float* dw_up,
+                               float* dw_down, void* workspace, size_t workspace_bytes,
+                               ptb_stream stream_, void* const* events, int32_t n_events) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   const void* ptrs[] = {dy, x, ln_gamma, w_qkv, w_o, w_up, w_down, dx,
                         dln_gamma, dln_beta, dw_qkv, dw_o, dw_up, dw_down};
   ptb_status st = check_layer(ptrs, 14, batch, seq, hidden, ffn, heads, window);
   if (st != PTB_OK) return st;
+  if (events && n_events != 7) return PTB_ERR_ARG;
+  if (events)
+    for (int i = 0; i < 7; ++i)
+      if (!events[i]) return PTB_ERR_ARG;
+  auto mark = [&](int i) -> bool {
+    if (!events) return true;
+    if (cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) == cudaSuccess) return true;
+    cudaGetLastError();  // the failed record must not be reported by a later launch
+    return false;
+  };
   const SavedLayout l = saved_layout(batch, seq, hidden, ffn, heads);
   st = check_saved(saved, saved_bytes, l);
   if (st != PTB_OK) return st;
@@ -1197,6 +1208,7 @@ ptb_status ptb_backward(const ptb_bf16* dy, const ptb_bf16* x, const ptb_bf16* l
   const size_t scratch_bytes = w.total - w.gemm;
 
   // 1. [dctx | dZ] = dy [W_o | W_down], dZ = dG * gelu'(Z) written into dU1
+  if (!mark(0)) return PTB_ERR_ARG;
   GemmCall c = call_dgrad_out(t, hidden, ffn);
   c.a0 = dy, c.b0 = w_o, c.b1 = w_down;
   c.out = dctx, c.ld_out = hidden, c.out1 = du1 + 3 * hidden, c.ld_out1 = ldu;
@@ -1204,32 +1216,52 @@ ptb_status ptb_backward(const ptb_bf16* dy, const ptb_bf16* x, const ptb_bf16* l
   st = gemm_call(ds, c, scratch, scratch_bytes, stream);
   if (st != PTB_OK) return st;
   // 2. [dW_o | dW_down] = dy^T [ctx | G]
+  if (!mark(1)) return PTB_ERR_ARG;
   c = call_wgrad_out(t, hidden, ffn, ldu);
   c.a0 = dy, c.b0 = ctx, c.b1 = u + 3 * hidden;
   c.out = dw_o, c.ld_out = hidden, c.out1 = dw_down, c.ld_out1 = ffn;
   st = gemm_call(ds, c, scratch, scratch_bytes, stream);
   if (st != PTB_OK) return st;
   // 3. [dQ | dK | dV] into dU1 from the banded attention backward
+  if (!mark(2)) return PTB_ERR_ARG;
   if (launch_swa_backward(swa_bwd_args(ds, u, ctx, dctx, du1, lse, delta, batch, seq, hidden, ffn,
                                        heads, window),
                           stream) != cudaSuccess)
     return PTB_ERR_LAUNCH;
   // 4. dxn = dU1 [W_qkv ; W_up]   (fp32)
+  if (!mark(3)) return PTB_ERR_ARG;
   c = call_dgrad_in(t, hidden, ffn, ldu);
   c.a0 = du1, c.a1 = du1 + 3 * hidden, c.b0 = w_qkv, c.b1 = w_up;
   c.out = dxn, c.ld_out = hidden;
   st = gemm_call(ds, c, scratch, scratch_bytes, stream);
   if (st != PTB_OK) return st;
   // 5. [dW_qkv ; dW_up] = dU1^T xn
+  if (!mark(4)) return PTB_ERR_ARG;
   c = call_wgrad_in(t, hidden, ffn, ldu);
   c.a0 = du1, c.b0 = xn;
   c.out = dw_qkv, c.ld_out = hidden, c.out1 = dw_up, c.ld_out1 = hidden;
   st = gemm_call(ds, c, scratch, scratch_bytes, stream);
   if (st != PTB_OK) return st;
   // 6. dx = dy + LN backward of dxn; dgamma, dbeta
-  return launch_status(launch_layernorm_backward(bf(x), bf(ln_gamma), stats, dxn, bf(dy), t,
-                                                 static_cast<int>(hidden), bf(dx), dln_gamma,
-                                                 dln_beta, ln_part, stream));
+  if (!mark(5)) return PTB_ERR_ARG;
+  st = launch_status(launch_layernorm_backward(bf(x), bf(ln_gamma), stats, dxn, bf(dy), t,
+                                               static_cast<int>(hidden), bf(dx), dln_gamma,
+                                               dln_beta, ln_part, stream));
+  if (st != PTB_OK) return st;
+  if (!mark(6)) return PTB_ERR_ARG;
+  return PTB_OK;
+}
+
+ptb_status ptb_backward(const ptb_bf16* dy, const ptb_bf16* x, const ptb_bf16* ln_gamma,
+                        const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
+                        const ptb_bf16* w_down, const void* saved, size_t saved_bytes,
+                        int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
+                        int32_t window, ptb_bf16* dx, float* dln_gamma, float* dln_beta,
+                        float* dw_qkv, float* dw_o, float* dw_up, float* dw_down, void* workspace,
+                        size_t workspace_bytes, ptb_stream stream) {
+  return ptb_backward_events(dy, x, ln_gamma, w_qkv, w_o, w_up, w_down, saved, saved_bytes, batch,
+                             seq, hidden, ffn, heads, window, dx, dln_gamma, dln_beta, dw_qkv,
+                             dw_o, dw_up, dw_down, workspace, workspace_bytes, stream, nullptr, 0);
 }
 
 ptb_status swa_attention_lse(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v,

@@ -264,6 +264,22 @@ ptb_status ptb_backward(const ptb_bf16* dy, const ptb_bf16* x, const ptb_bf16* l
                         int32_t window, ptb_bf16* dx, float* dln_gamma, float* dln_beta,
                         float* dw_qkv, float* dw_o, float* dw_up, float* dw_down, void* workspace,
                         size_t workspace_bytes, ptb_stream stream);
+/*
+ * ptb_backward that also records seven caller-owned CUDA events (cudaEvent_t
+ * passed as void*) on `stream`: before the [out | down] input-gradient GEMM,
+ * the [out | down] weight-gradient GEMM, the attention backward, the
+ * [QKV | up] input-gradient GEMM, the [QKV | up] weight-gradient GEMM and
+ * the LayerNorm backward, and after it.  n_events must be 7; a null event or
+ * a failed record returns PTB_ERR_ARG.
+ */
+ptb_status ptb_backward_events(const ptb_bf16* dy, const ptb_bf16* x, const ptb_bf16* ln_gamma,
+                               const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
+                               const ptb_bf16* w_down, const void* saved, size_t saved_bytes,
+                               int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,
+                               int32_t heads, int32_t window, ptb_bf16* dx, float* dln_gamma,
+                               float* dln_beta, float* dw_qkv, float* dw_o, float* dw_up,
+                               float* dw_down, void* workspace, size_t workspace_bytes,
+                               ptb_stream stream, void* const* events, int32_t n_events);
 
 /* Frees the library's own workspace arena on the current device (if any). */
 ptb_status ptb_release_workspace(void);

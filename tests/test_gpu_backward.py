@@ -54,7 +54,8 @@ ZERO_TOL = 1e-4
 
 def assert_grad_close(got, want, what):
     if not to_np(want).any():
-        mx = float(np.abs(to_np(got)).max()) if got.numel() else 0.0
+        g = to_np(got)
+        mx = float(np.abs(g).max()) if g.size else 0.0
         print(f"{what}: closed-form zero, max |got| {mx:.3e}")
         assert mx <= ZERO_TOL, f"{what}: max |got| {mx:.3e} where the gradient is 0"
         return
@@ -185,3 +186,61 @@ def test_backward_zero_output_weights(ptb_lib):
     assert torch.equal(g["dx"].cpu(), dy)
     for name in ("dln_gamma", "dln_beta", "dw_qkv", "dw_up"):
         assert not g[name].any(), name
+
+
+# ------------------------------------------------------- full size --
+
+def _train_on_device(ptb_lib, cfg, dy_seed):
+    """forward_train + backward on the device with caller workspaces, as the
+    training benchmark launches them; returns host copies of inputs, dy and
+    the gradients."""
+    d = workloads.ptb_inputs(cfg, device="cuda")
+    dy = workloads.normal_bf16(tuple(d["x"].shape), seed=dy_seed, device="cuda")
+    b, s, h, f = cfg.batch, cfg.seq, cfg.hidden, cfg.ffn
+    ws_f = torch.empty(ptb_lib.workspace_size(b, s, h, f), dtype=torch.uint8, device="cuda")
+    ws_b = torch.empty(ptb_lib.backward_workspace_size(b, s, h, f, cfg.heads), dtype=torch.uint8,
+                       device="cuda")
+    w = (d["w_qkv"], d["w_o"], d["w_up"], d["w_down"])
+    _, saved = ptb_lib.ptb_forward_train(d["x"], d["ln_gamma"], d["ln_beta"], *w, cfg.heads,
+                                         cfg.window, workspace=ws_f)
+    g = ptb_lib.ptb_backward(dy, d["x"], d["ln_gamma"], *w, saved, cfg.heads, cfg.window,
+                             workspace=ws_b)
+    torch.cuda.synchronize()
+    host = {k: v.cpu() for k, v in d.items()}
+    g = {k: v.cpu() for k, v in g.items()}
+    dy = dy.cpu()
+    del d, ws_f, ws_b, saved, w
+    torch.cuda.empty_cache()
+    return host, dy, g
+
+
+def test_ptb_backward_full_size_13b(ptb_lib):
+    cfg = workloads.PTB_CONFIGS["13b"]
+    host, dy, g = _train_on_device(ptb_lib, cfg, cfg.seed + 100)
+    want = oracle.ptb_backward(host["x"], host["ln_gamma"], host["ln_beta"], host["w_qkv"],
+                               host["w_o"], host["w_up"], host["w_down"], cfg.heads, cfg.window,
+                               dy)
+    for name in GRADS:
+        assert_grad_close(g[name], want[name], f"13b {name}")
+
+
+@pytest.mark.parametrize("name", ["175b"])
+def test_ptb_backward_full_size_sampled(ptb_lib, name):
+    """dx at sampled rows and the weight gradients at two heads, 48 FFN
+    columns and 32 output rows, each against the oracle's formula on those
+    entries (tests/backward_sampled)."""
+    from tests.backward_sampled import gathered, sampled_backward
+    cfg = workloads.PTB_CONFIGS[name]
+    host, dy, g = _train_on_device(ptb_lib, cfg, cfg.seed + 100)
+    rng = np.random.default_rng(cfg.seed)
+    rows = workloads.sample_rows(cfg.seq, cfg.window)
+    head_sel = [0, cfg.heads - 1]
+    f_sel = sorted(rng.choice(cfg.ffn, 48, replace=False).tolist())
+    r_sel = sorted(rng.choice(cfg.hidden, 32, replace=False).tolist())
+    want = sampled_backward(host["x"], host["ln_gamma"], host["ln_beta"], host["w_qkv"],
+                            host["w_o"], host["w_up"], host["w_down"], cfg.heads, cfg.window, dy,
+                            rows, head_sel, f_sel, r_sel)
+    got = gathered({k: to_np(v) for k, v in g.items()}, cfg.hidden, cfg.heads, rows, head_sel,
+                   f_sel, r_sel)
+    for k in want:
+        assert_grad_close(got[k], want[k], f"{name} {k} (sampled)")

@@ -202,3 +202,23 @@ def test_planted_backward_mistake_is_caught(monkeypatch, name, bad, check):
     monkeypatch.setattr(oracle, name, bad)
     with pytest.raises(AssertionError):
         check()
+
+
+def test_sampled_backward_helper_matches_full_oracle():
+    """The full-size tests' sampled gradient entries (tests/backward_sampled)
+    are the full backward oracle's entries."""
+    from tests.backward_sampled import gathered, sampled_backward
+    heads, window = 4, 5
+    r = np.random.default_rng(9)
+    p = dict(x=r.standard_normal((2, 23, 16)), ln_gamma=1 + 0.1 * r.standard_normal(16),
+             ln_beta=0.1 * r.standard_normal(16), w_qkv=0.3 * r.standard_normal((48, 16)),
+             w_o=0.3 * r.standard_normal((16, 16)), w_up=0.3 * r.standard_normal((40, 16)),
+             w_down=0.3 * r.standard_normal((16, 40)))
+    dy = r.standard_normal((2, 23, 16))
+    args = [p[n] for n in NAMES] + [heads, window, dy]
+    full = oracle.ptb_backward(*args)
+    rows, head_sel, f_sel, r_sel = [0, 4, 5, 22], [1, 3], [0, 7, 39], [2, 15]
+    want = gathered(full, 16, heads, rows, head_sel, f_sel, r_sel)
+    got = sampled_backward(*args, rows, head_sel, f_sel, r_sel)
+    for k in want:
+        assert np.allclose(got[k], want[k], rtol=1e-12, atol=1e-12), k
