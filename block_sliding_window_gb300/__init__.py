@@ -23,7 +23,7 @@ __all__ = [
     "wait_probe", "serial_forward", "serial_workspace_size", "prepare_fp8_weights",
     "fp8_workspace_size", "ptb_forward_fp8", "ptb_forward_fp8_events", "train_saved_size",
     "ptb_forward_train", "backward_workspace_size", "ptb_backward", "ptb_backward_events", "swa_attention_lse",
-    "swa_attention_backward", "LIB_PATH", "SYMBOLS",
+    "swa_attention_backward", "set_gemm_pairs", "LIB_PATH", "SYMBOLS",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libptb.so")
@@ -52,6 +52,7 @@ SYMBOLS = {
     "ptb_forward_train": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p, _sz, _p]),
     "ptb_backward_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i32]),
     "ptb_backward": (_st, [_p] * 8 + [_sz] + [_i64] * 4 + [_i32, _i32] + [_p] * 8 + [_sz, _p]),
+    "ptb_set_gemm_pairs": (_st, [_i32, _p]),
     "ptb_backward_events": (_st, [_p] * 8 + [_sz] + [_i64] * 4 + [_i32, _i32] + [_p] * 8
                             + [_sz, _p, _p, _i32]),
     "swa_attention_lse": (_st, [_p, _p, _p, _i64, _i32, _i64, _i32, _i32, ctypes.c_float, _p, _p,
@@ -323,6 +324,14 @@ def swa_attention_counts(q, k, v, window: int, scale: float = 0.0, stream=None):
                                   _ptr(o), _ptr(counts), _stream(stream))
     _check(st, "swa_attention_counts")
     return o, counts
+
+
+def set_gemm_pairs(mode: int) -> int:
+    """GEMM tile mode on the current device: 1 CTA pairs (256 x 256 tiles), 0
+    single CTAs, -1 automatic; returns the previous mode."""
+    prev = ctypes.c_int32(0)
+    _check(load().ptb_set_gemm_pairs(mode, ctypes.byref(prev)), "ptb_set_gemm_pairs")
+    return prev.value
 
 
 def train_saved_size(batch: int, seq: int, hidden: int, ffn: int, heads: int) -> int:

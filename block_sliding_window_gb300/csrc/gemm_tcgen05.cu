@@ -74,27 +74,26 @@ struct Unit {
   int tile, kb0, kb1, slot;
 };
 
-// The i-th unit of this CTA; false when the CTA has no more work.
+// The i-th unit of worker `self` of `count` (a CTA, or a CTA pair); false
+// when the worker has no more work.
 __device__ __forceinline__ bool unit_at(const GemmArgs& p, int num_tiles, int num_kb, int i,
-                                        Unit& u) {
-  const int grid = gridDim.x;
+                                        Unit& u, int self, int count) {
   if (p.split_s < 2) {
-    const int tile = blockIdx.x + i * grid;
+    const int tile = self + i * count;
     if (tile >= num_tiles) return false;
     u = {tile, 0, num_kb, -1};
     return true;
   }
-  const int whole = num_tiles - p.split_r;  // a multiple of grid
-  const int n_whole = whole / grid;
+  const int whole = num_tiles - p.split_r;  // a multiple of count
+  const int n_whole = whole / count;
   if (i < n_whole) {
-    u = {static_cast<int>(blockIdx.x) + i * grid, 0, num_kb, -1};
+    u = {self + i * count, 0, num_kb, -1};
     return true;
   }
-  if (i == n_whole && static_cast<int>(blockIdx.x) < p.split_r * p.split_s) {
-    const int r = blockIdx.x / p.split_s;
-    const int s = blockIdx.x % p.split_s;
-    u = {whole + r, s * num_kb / p.split_s, (s + 1) * num_kb / p.split_s,
-         static_cast<int>(blockIdx.x)};
+  if (i == n_whole && self < p.split_r * p.split_s) {
+    const int r = self / p.split_s;
+    const int s = self % p.split_s;
+    u = {whole + r, s * num_kb / p.split_s, (s + 1) * num_kb / p.split_s, self};
     return true;
   }
   return false;
@@ -204,14 +203,88 @@ __device__ __forceinline__ void store_chunk(const GemmArgs& p, int row, int col,
 }
 
 // Output tile origin of tile index t (M index fastest, or N index fastest).
-__device__ __forceinline__ void tile_origin(const GemmArgs& p, int t, int num_m, int num_n, int bn,
-                                            int& m0, int& n0) {
+__device__ __forceinline__ void tile_origin(const GemmArgs& p, int t, int num_m, int num_n, int bm,
+                                            int bn, int& m0, int& n0) {
   if (p.n_fastest) {
-    m0 = (t / num_n) * BM;
+    m0 = (t / num_n) * bm;
     n0 = (t % num_n) * bn;
   } else {
-    m0 = (t % num_m) * BM;
+    m0 = (t % num_m) * bm;
     n0 = (t / num_m) * bn;
+  }
+}
+
+// The epilogue of one unit for one thread's output row `row`: a whole tile
+// goes straight from TMEM through store_chunk; a K piece of a split tile
+// publishes its fp32 partial (row `prow` of the ROWS-row partial tile) and
+// counts its warp's arrival on p.counters[counter], and the warp that
+// arrives last for those 32 rows sums all pieces in piece order and stores.
+template <int BN, int EPI, bool FP8, int ROWS>
+__device__ __forceinline__ void epilogue_unit(const GemmArgs& p, const Unit& u, int row, int prow,
+                                              int counter, uint32_t t_row, int n0, int lane) {
+  bool finish = true;
+  if (u.slot >= 0) {
+    // A K piece: publish the fp32 partial, then count the arrival.
+    float* mine = p.partials + (static_cast<int64_t>(u.slot) * ROWS + prow) * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(t_row + c, r);
+      tmem_ld_wait();
+      float4* dst = reinterpret_cast<float4*>(mine + c);
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        __stcg(dst + v, make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                    __uint_as_float(r[4 * v + 2]),
+                                    __uint_as_float(r[4 * v + 3])));
+    }
+    // Each warp owns its 32 rows: it counts its own arrival for that
+    // quarter of the tile, and the last warp to arrive for the quarter
+    // finishes those rows.  No warp waits for another.
+    __threadfence();
+    __syncwarp();
+    unsigned prev = 0;
+    if (lane == 0) prev = atomicAdd(p.counters + counter, 1u);
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    finish = prev == static_cast<unsigned>(p.split_s - 1);
+    if (finish) __threadfence();
+  }
+  if (finish && u.slot < 0) {
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(t_row + c, r);
+      tmem_ld_wait();
+      float acc[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
+      if constexpr (FP8) dequantize(p, row, n0 + c, acc);
+      if (row < p.M) store_chunk<EPI>(p, row, n0 + c, acc);
+    }
+  } else if (finish) {
+    // Sum every piece's partial (this warp's own included) in piece order,
+    // so the result does not depend on which warp happened to finish.
+    const int group0 = (u.slot / p.split_s) * p.split_s;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      float acc[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+      for (int s = 0; s < p.split_s; ++s) {
+        const float4* src = reinterpret_cast<const float4*>(
+            p.partials + (static_cast<int64_t>(group0 + s) * ROWS + prow) * BN + c);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float4 q = __ldcg(src + v);
+          acc[4 * v] += q.x;
+          acc[4 * v + 1] += q.y;
+          acc[4 * v + 2] += q.z;
+          acc[4 * v + 3] += q.w;
+        }
+      }
+      if constexpr (FP8) dequantize(p, row, n0 + c, acc);
+      if (row < p.M) store_chunk<EPI>(p, row, n0 + c, acc);
+    }
   }
 }
 
@@ -288,9 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       uint32_t armed_parity = 0;
       bool ok = true;
       Unit u;
-      for (int i = 0; ok && unit_at(p, num_tiles, num_kb, i, u); ++i) {
+      for (int i = 0; ok && unit_at(p, num_tiles, num_kb, i, u, blockIdx.x, gridDim.x); ++i) {
         int m0, n0;
-        tile_origin(p, u.tile, num_m, num_n, BN, m0, n0);
+        tile_origin(p, u.tile, num_m, num_n, BM, BN, m0, n0);
         const bool nlo = n0 < p.n_split;
         const int by = nlo ? n0 : n0 - p.n_split;
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
@@ -346,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       uint32_t phase = 0;
       bool ok = true;
       Unit u;
-      for (int i = 0; ok && unit_at(p, num_tiles, num_kb, i, u); ++i) {
+      for (int i = 0; ok && unit_at(p, num_tiles, num_kb, i, u, blockIdx.x, gridDim.x); ++i) {
         const int acc = i & 1;
         const uint32_t acc_phase = (i >> 1) & 1;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
@@ -393,80 +466,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int quarter = warp & 3;
     const int row_local = quarter * 32 + lane;
     Unit u;
-    for (int i = 0; unit_at(p, num_tiles, num_kb, i, u); ++i) {
+    for (int i = 0; unit_at(p, num_tiles, num_kb, i, u, blockIdx.x, gridDim.x); ++i) {
       const int acc_buf = i & 1;
       const uint32_t acc_phase = (i >> 1) & 1;
       if (!mbar_wait_warp(&tfull_bar[acc_buf], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
       int m0, n0;
-      tile_origin(p, u.tile, num_m, num_n, BN, m0, n0);
+      tile_origin(p, u.tile, num_m, num_n, BM, BN, m0, n0);
       const int row = m0 + row_local;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc_buf * BN);
-      bool finish = true;
-      if (u.slot >= 0) {
-        // A K piece: publish the fp32 partial, then count the arrival.
-        float* mine = p.partials + (static_cast<int64_t>(u.slot) * BM + row_local) * BN;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + c, r);
-          tmem_ld_wait();
-          float4* dst = reinterpret_cast<float4*>(mine + c);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            __stcg(dst + v, make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                        __uint_as_float(r[4 * v + 2]),
-                                        __uint_as_float(r[4 * v + 3])));
-        }
-        // Each warp owns its 32 rows: it counts its own arrival for that
-        // quarter of the tile, and the last warp to arrive for the quarter
-        // finishes those rows.  No warp waits for another.
-        __threadfence();
-        __syncwarp();
-        unsigned prev = 0;
-        if (lane == 0) prev = atomicAdd(p.counters + (u.slot / p.split_s) * 4 + quarter, 1u);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        finish = prev == static_cast<unsigned>(p.split_s - 1);
-        if (finish) __threadfence();
-      }
-      if (finish && u.slot < 0) {
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + c, r);
-          tmem_ld_wait();
-          float acc[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
-          if constexpr (FP8) dequantize(p, row, n0 + c, acc);
-          if (row < p.M) store_chunk<EPI>(p, row, n0 + c, acc);
-        }
-      } else if (finish) {
-        // Sum every piece's partial (this warp's own included) in piece order,
-        // so the result does not depend on which warp happened to finish.
-        const int group0 = (u.slot / p.split_s) * p.split_s;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          float acc[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-          for (int s = 0; s < p.split_s; ++s) {
-            const float4* src = reinterpret_cast<const float4*>(
-                p.partials + (static_cast<int64_t>(group0 + s) * BM + row_local) * BN + c);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const float4 q = __ldcg(src + v);
-              acc[4 * v] += q.x;
-              acc[4 * v + 1] += q.y;
-              acc[4 * v + 2] += q.z;
-              acc[4 * v + 3] += q.w;
-            }
-          }
-          if constexpr (FP8) dequantize(p, row, n0 + c, acc);
-          if (row < p.M) store_chunk<EPI>(p, row, n0 + c, acc);
-        }
-      }
+      epilogue_unit<BN, EPI, FP8, BM>(p, u, row, row_local, (u.slot / p.split_s) * 4 + quarter,
+                                      t_row, n0, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc_buf]);
@@ -480,6 +491,272 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
+}
+
+// ------------------------------------------------------------ CTA pairs --
+// 256 x 256 output tiles on a CTA pair (a cluster of two CTAs on the two SMs
+// of a TPC, tcgen05 cta_group::2).  Rank r loads rows m0 + 128 r of A and
+// columns by + 128 r of B into its own shared memory; rank 0 issues M = 256,
+// N = 256 MMAs that read both CTAs' tiles at the same offsets, and each CTA's
+// TMEM receives its 128 rows of the accumulator.  Per SM and 64-wide k-block
+// the stage is 32 KB instead of 48 KB, so the shared-memory traffic of TMA
+// writes plus operand reads drops by a third.
+//   warp 0      both ranks: TMA producer into their own 6-stage ring.  The
+//               copies of both ranks complete on rank 0's `full` barrier of
+//               the stage (cta_group::2 TMA), which rank 0 arms with the
+//               bytes of both.  (A first version relayed rank 1's stages with
+//               a cluster-scope release arrive per stage and ran at 31%
+//               tensor activity.)
+//   warp 1      both ranks allocate TMEM together (cta_group::2).  Rank 0
+//               issues the MMAs and commits stage and tile completion to the
+//               barriers at the same offset in both CTAs.
+//   warps 2..5  both ranks: epilogue of their 128 rows; each warp then
+//               arrives on rank 0's `tempty` barrier (8 arrivals per tile).
+// The remainder wave is split along K per pair as in the single-CTA kernel
+// (256-row partial tiles, 8 arrival counters per tile).
+constexpr int kPairBN = 256;
+constexpr int kPairStages = 6;
+struct PairCfg {
+  static constexpr int kABytes = BM * 128;
+  static constexpr int kBBytes = (kPairBN / 2) * 128;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * kPairBN;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = kPairStages * kStageBytes + kBarBytes + 1024;
+};
+
+template <int EPI, int LAYOUT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ GemmArgs p) {
+  using C = PairCfg;
+  constexpr int BN = kPairBN;
+  constexpr int BK = 64;
+  constexpr int NS = kPairStages;
+  // MN-major operands arrive as 64-wide MN blocks of 64 K rows (8 KB each).
+  constexpr bool kAmn = (LAYOUT & 1) != 0;
+  constexpr bool kBmn = (LAYOUT & 2) != 0;
+  constexpr uint32_t kMnBlock = 64 * 128;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + NS * C::kStageBytes);
+  uint64_t* empty_bar = full_bar + NS;
+  uint64_t* tfull_bar = empty_bar + NS;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* done_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const uint32_t rank = cluster_ctarank();
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int npairs = static_cast<int>(gridDim.x >> 1);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_m = (p.M + 2 * BM - 1) / (2 * BM);
+  const int num_n = p.N / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full_bar[s], 1);  // used in rank 0 only
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 8);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.a0);
+    tma_prefetch_desc(&p.a1);
+    tma_prefetch_desc(&p.b0);
+    tma_prefetch_desc(&p.b1);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before anything crosses the pair
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto stage_a = [&](int s) { return smem + s * C::kStageBytes; };
+  auto stage_b = [&](int s) { return smem + s * C::kStageBytes + C::kABytes; };
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      const uint64_t pol = p.a_keep ? l2_policy_evict_last() : l2_policy_evict_first();
+      const uint64_t pol_b = p.b_keep ? l2_policy_evict_last() : l2_policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      bool ok = true;
+      Unit u;
+      for (int i = 0; ok && unit_at(p, num_tiles, num_kb, i, u, pair, npairs); ++i) {
+        int m0, n0;
+        tile_origin(p, u.tile, num_m, num_n, 2 * BM, BN, m0, n0);
+        const bool nlo = n0 < p.n_split;
+        const int by = (nlo ? n0 : n0 - p.n_split) + static_cast<int>(rank) * (BN / 2);
+        const int my_m = m0 + static_cast<int>(rank) * BM;
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const int k = kb * BK;
+          const bool klo = k < p.k_split;
+          const int kx = klo ? k : k - p.k_split;
+          const uint32_t leader_full = cluster_map(&full_bar[stage], 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::kStageBytes);
+          const CUtensorMap* amap = klo ? &p.a0 : &p.a1;
+          const CUtensorMap* bmap = (nlo && klo) ? &p.b0 : &p.b1;
+          if constexpr (kAmn) {
+#pragma unroll
+            for (int h = 0; h < BM / 64; ++h)
+              tma_load_2d_pair(stage_a(stage) + h * kMnBlock, amap, leader_full, my_m + 64 * h,
+                               kx, pol);
+          } else {
+            tma_load_2d_pair(stage_a(stage), amap, leader_full, kx, my_m, pol);
+          }
+          if constexpr (kBmn) {
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              tma_load_2d_pair(stage_b(stage) + h * kMnBlock, bmap, leader_full, by + 64 * h, kx,
+                               pol_b);
+          } else {
+            tma_load_2d_pair(stage_b(stage), bmap, leader_full, kx, by, pol_b);
+          }
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == NS) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Unwinding: let every copy this thread issued land before the CTA
+        // (and its shared memory) goes away.  Rank 0 waits for its stages;
+        // rank 1's completions go to rank 0, so it gives them 100 us.
+        volatile int no_abort = 0;
+        if (rank == 0) {
+          for (int s = 0; s < NS; ++s)
+            if (armed & (1u << s))
+              mbar_wait(&full_bar[s], (armed_parity >> s) & 1u, &no_abort, p.status);
+        } else {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 100000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ----------------------------------------------------- MMA issuer --
+      constexpr uint32_t idesc = umma_idesc_bf16(2 * BM, BN) | (kAmn ? 1u << 15 : 0u) |
+                                 (kBmn ? 1u << 16 : 0u);
+      constexpr uint64_t kStepA = kAmn ? 128 : 2;
+      constexpr uint64_t kStepB = kBmn ? 128 : 2;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      Unit u;
+      for (int i = 0; ok && unit_at(p, num_tiles, num_kb, i, u, pair, npairs); ++i) {
+        const int acc = i & 1;
+        const uint32_t acc_phase = (i >> 1) & 1;
+        if (!mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+          if (!mbar_wait_cluster(&full_bar[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = kAmn ? sw128_mnmajor_desc(smem_addr(stage_a(stage)), kMnBlock)
+                                      : sw128_kmajor_desc(smem_addr(stage_a(stage)));
+          const uint64_t bdesc = kBmn ? sw128_mnmajor_desc(smem_addr(stage_b(stage)), kMnBlock)
+                                      : sw128_kmajor_desc(smem_addr(stage_b(stage)));
+#pragma unroll
+          for (int kk = 0; kk < kMmasPerBlock; ++kk)
+            umma_bf16_pair(d_tmem, adesc + kStepA * kk, bdesc + kStepB * kk, idesc,
+                           (kb != u.kb0 || kk != 0) ? 1u : 0u);
+          umma_commit_pair(&empty_bar[stage], 0x3);
+          if (++stage == NS) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit_pair(&tfull_bar[acc], 0x3);
+      }
+      // Every MMA this thread issued completes before TMEM is released in
+      // either CTA.
+      umma_commit_pair(done_bar, 0x3);
+      volatile int no_abort = 0;
+      mbar_wait(done_bar, 0, &no_abort, p.status);
+    } else if (lane == 0) {
+      // The pair's MMAs read this CTA's shared memory and write its TMEM:
+      // wait for the last of them (rank 0 always commits this barrier).
+      volatile int no_abort = 0;
+      mbar_wait(done_bar, 0, &no_abort, p.status);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue --
+    const int quarter = warp & 3;
+    const int row_local = quarter * 32 + lane;
+    Unit u;
+    for (int i = 0; unit_at(p, num_tiles, num_kb, i, u, pair, npairs); ++i) {
+      const int acc_buf = i & 1;
+      const uint32_t acc_phase = (i >> 1) & 1;
+      if (!mbar_wait_cluster_warp(&tfull_bar[acc_buf], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      int m0, n0;
+      tile_origin(p, u.tile, num_m, num_n, 2 * BM, BN, m0, n0);
+      const int prow = static_cast<int>(rank) * BM + row_local;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc_buf * BN);
+      epilogue_unit<BN, EPI, false, 2 * BM>(
+          p, u, m0 + prow, prow, (u.slot / p.split_s) * 8 + static_cast<int>(rank) * 4 + quarter,
+          t_row, n0, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(cluster_map(&tempty_bar[acc_buf], 0));
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // nothing of either CTA still signals the other
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int EPI, int LAYOUT>
+cudaError_t launch_pair(const GemmArgs& a, cudaStream_t stream) {
+  using C = PairCfg;
+  auto kern = gemm_pair_kernel<EPI, LAYOUT>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  if (a.grid % 2) return cudaErrorInvalidValue;
+  kern<<<a.grid, kThreads, C::kSmemBytes, stream>>>(a);
+  return cudaGetLastError();
 }
 
 template <int BN, int EPI, bool FP8, int LAYOUT>
@@ -501,7 +778,7 @@ cudaError_t launch_typed(const GemmArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-GemmPlan plan_gemm(int64_t tiles, int64_t num_kb, int sms, int block_n) {
+GemmPlan plan_gemm(int64_t tiles, int64_t num_kb, int sms, int block_n, int rows) {
   GemmPlan g;
   g.grid = static_cast<int>(tiles < sms ? tiles : sms);
   g.split_r = 0;
@@ -518,8 +795,8 @@ GemmPlan plan_gemm(int64_t tiles, int64_t num_kb, int sms, int block_n) {
       if (tiles < sms) g.grid = static_cast<int>(r * s);
     }
   }
-  g.partial_bytes = static_cast<size_t>(g.split_r) * g.split_s * BM * block_n * sizeof(float);
-  g.counter_bytes = static_cast<size_t>(g.split_r) * 4 * sizeof(unsigned);
+  g.partial_bytes = static_cast<size_t>(g.split_r) * g.split_s * rows * block_n * sizeof(float);
+  g.counter_bytes = static_cast<size_t>(g.split_r) * (rows / 32) * sizeof(unsigned);
   return g;
 }
 
@@ -539,8 +816,23 @@ cudaError_t launch_bn(const GemmArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (a.split_s >= 2 && a.split_r > 0) {
-    cudaError_t e = cudaMemsetAsync(a.counters, 0, a.split_r * 4 * sizeof(unsigned), stream);
+    cudaError_t e =
+        cudaMemsetAsync(a.counters, 0, a.split_r * (a.pair ? 8 : 4) * sizeof(unsigned), stream);
     if (e != cudaSuccess) return e;
+  }
+  if (a.pair) {  // bf16, 256-wide N tiles on CTA pairs
+    if (a.fp8 || a.block_n != kPairBN) return cudaErrorInvalidValue;
+    if (a.layout == kLayoutKK && a.epilogue == kEpiQkvGelu)
+      return launch_pair<kEpiQkvGelu, kLayoutKK>(a, stream);
+    if (a.layout == kLayoutKK && a.epilogue == kEpiResidual)
+      return launch_pair<kEpiResidual, kLayoutKK>(a, stream);
+    if (a.layout == kLayoutKN && a.epilogue == kEpiDgelu)
+      return launch_pair<kEpiDgelu, kLayoutKN>(a, stream);
+    if (a.layout == kLayoutKN && a.epilogue == kEpiF32)
+      return launch_pair<kEpiF32, kLayoutKN>(a, stream);
+    if (a.layout == kLayoutNN && a.epilogue == kEpiF32)
+      return launch_pair<kEpiF32, kLayoutNN>(a, stream);
+    return cudaErrorInvalidValue;
   }
   // The instantiated (epilogue, operand type, layout) combinations: the
   // forward GEMMs (bf16 and e4m3, K-major) and the backward GEMMs (bf16).

@@ -45,6 +45,7 @@ struct GemmArgs {
   int layout;   // GemmLayout
   int n_fastest;  // tile order: 0 = M index fastest, 1 = N index fastest
   int a_keep, b_keep;  // L2 priority of the operand's loads: 1 evict_last, 0 evict_first
+  int pair;  // 1: 256 x 256 tiles on CTA pairs (grid = 2 x pairs); bf16, K-major, block_n 256
   // Output: element (row, col) goes to out[row, col] (row stride ld_out),
   // except that columns >= out_split_col go to out1[row, col - out_split_col]
   // and rows >= out_split_row to out1[row - out_split_row, col] (row stride
@@ -88,7 +89,9 @@ struct GemmPlan {
 // Grid and K split for `tiles` output tiles of `num_kb` k-blocks on `sms`
 // SMs: whole waves of tiles, then the remainder tiles split along K over the
 // SMs the last wave would leave idle.
-GemmPlan plan_gemm(int64_t tiles, int64_t num_kb, int sms, int block_n);
+// `workers` is the number of CTAs (or CTA pairs), `rows` the tile height
+// (128, or 256 for pairs).
+GemmPlan plan_gemm(int64_t tiles, int64_t num_kb, int workers, int block_n, int rows = 128);
 
 struct SwaArgs {
   const __nv_bfloat16 *q, *k, *v;

@@ -281,7 +281,21 @@ ptb_status ptb_backward_events(const ptb_bf16* dy, const ptb_bf16* x, const ptb_
                                float* dw_down, void* workspace, size_t workspace_bytes,
                                ptb_stream stream, void* const* events, int32_t n_events);
 
-/* Frees the library's own workspace arena on the current device (if any). */
+/*
+ * ptb_set_gemm_pairs: tile shape of the bf16 GEMMs on the current device.
+ * 1: 256 x 256 tiles on CTA pairs (a cluster of two CTAs on one TPC, tcgen05
+ * cta_group::2) wherever the GEMM has 256-wide N tiles; 0: 128 x N tiles on
+ * single CTAs; -1 (the default, or PTB_GEMM_PAIRS=0 / 1 in the environment
+ * at first use): pairs in ptb_forward_train and ptb_backward, and in the
+ * forward-only calls for GEMMs of at most 2^39 multiply-adds (larger
+ * forward-only layers run at the GPU's power cap, where pairs gain nothing
+ * and the lower clock slows the other kernels).  The results agree within rounding
+ * (the last wave's K split may differ).  *previous (if not null) receives
+ * the old mode.  PTB_ERR_ARG for another mode.
+ */
+ptb_status ptb_set_gemm_pairs(int32_t mode, int32_t* previous);
+
+/* Frees the library's own workspace arena/* Frees the library's own workspace arena on the current device (if any). */
 ptb_status ptb_release_workspace(void);
 
 /*

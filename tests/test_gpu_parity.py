@@ -386,3 +386,56 @@ def test_ptb_forward_full_size_sampled(ptb_lib, name):
           f"bf16-storage floor {floor:.3e}, bound {bound:.3e}")
     assert rel <= REL_L2, f"{name}: rel-L2 {rel:.3e}"
     assert ex <= bound, f"{name}: max-abs beyond rounding {ex:.3e} > {bound:.3e}"
+
+
+# ------------------------------------------------ GEMM tile shapes --
+
+@pytest.fixture
+def gemm_pairs(ptb_lib, request):
+    prev = ptb_lib.set_gemm_pairs(request.param)
+    yield request.param
+    ptb_lib.set_gemm_pairs(prev)
+
+
+@pytest.mark.parametrize("gemm_pairs", [0, 1], indirect=True, ids=["single", "pairs"])
+@pytest.mark.parametrize("cfg", [workloads.small_ptb(2, 300, 256, 4, 1024, 100, seed=41),
+                                 workloads.small_ptb(1, 520, 512, 4, 2048, 300, seed=42)],
+                         ids=lambda c: c.name)
+def test_ptb_forward_both_gemm_tile_shapes(ptb_lib, gemm_pairs, cfg):
+    """The layer with 128 x 256 single-CTA tiles and with 256 x 256 CTA-pair
+    tiles (ragged last M tile included) against the oracle."""
+    host = workloads.ptb_inputs(cfg)
+    d = _cuda(host)
+    y = ptb_lib.ptb_forward(d["x"], d["ln_gamma"], d["ln_beta"], d["w_qkv"], d["w_o"],
+                            d["w_up"], d["w_down"], cfg.heads, cfg.window)
+    torch.cuda.synchronize()
+    want = oracle.ptb_forward(host["x"], host["ln_gamma"], host["ln_beta"], host["w_qkv"],
+                              host["w_o"], host["w_up"], host["w_down"], cfg.heads, cfg.window)
+    assert_close(y, want, f"{cfg.name} pairs={gemm_pairs}")
+
+
+@pytest.mark.parametrize("gemm_pairs", [1], indirect=True, ids=["pairs"])
+def test_ptb_forward_full_size_pairs_175b(ptb_lib, gemm_pairs):
+    """CTA-pair tiles forced on the 175B-shaped layer (the automatic mode uses
+    single-CTA tiles there): 2688 and 384 pair tiles, the second GEMM's last
+    wave split along K over all 76 pairs."""
+    cfg = workloads.PTB_CONFIGS["175b"]
+    d = workloads.ptb_inputs(cfg, device="cuda")
+    ws = torch.empty(ptb_lib.workspace_size(cfg.batch, cfg.seq, cfg.hidden, cfg.ffn),
+                     dtype=torch.uint8, device="cuda")
+    y = ptb_lib.ptb_forward(d["x"], d["ln_gamma"], d["ln_beta"], d["w_qkv"], d["w_o"], d["w_up"],
+                            d["w_down"], cfg.heads, cfg.window, workspace=ws)
+    torch.cuda.synchronize()
+    rows = workloads.sample_rows(cfg.seq, cfg.window)
+    host = {k: v.cpu() for k, v in d.items()}
+    del d, ws
+    want = oracle.ptb_forward(host["x"], host["ln_gamma"], host["ln_beta"], host["w_qkv"],
+                              host["w_o"], host["w_up"], host["w_down"], cfg.heads, cfg.window,
+                              rows=rows)
+    model = ptb_forward_bf16_storage(host["x"], host["ln_gamma"], host["ln_beta"], host["w_qkv"],
+                                     host["w_o"], host["w_up"], host["w_down"], cfg.heads,
+                                     cfg.window, rows)
+    _, _, floor = errors(model, want[0])
+    rel, mx, ex = errors(y[0, rows], want[0])
+    print(f"175b pairs: rel-L2 {rel:.3e}, max-abs {mx:.3e}, beyond rounding {ex:.3e}")
+    assert rel <= REL_L2 and ex <= max(MAX_ABS, 1.25 * floor)
