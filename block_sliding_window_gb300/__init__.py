@@ -23,7 +23,7 @@ __all__ = [
     "wait_probe", "serial_forward", "serial_workspace_size", "prepare_fp8_weights",
     "fp8_workspace_size", "ptb_forward_fp8", "ptb_forward_fp8_events", "train_saved_size",
     "ptb_forward_train", "backward_workspace_size", "ptb_backward", "ptb_backward_events", "swa_attention_lse",
-    "swa_attention_backward", "set_gemm_pairs", "LIB_PATH", "SYMBOLS",
+    "swa_attention_backward", "set_gemm_pairs", "host_workspace_size", "ptb_forward_host", "LIB_PATH", "SYMBOLS",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libptb.so")
@@ -53,6 +53,8 @@ SYMBOLS = {
     "ptb_backward_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i32]),
     "ptb_backward": (_st, [_p] * 8 + [_sz] + [_i64] * 4 + [_i32, _i32] + [_p] * 8 + [_sz, _p]),
     "ptb_set_gemm_pairs": (_st, [_i32, _p]),
+    "ptb_forward_host_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
+    "ptb_forward_host": (_st, [_p] * 7 + [_i64] * 4 + [_i32, _i32, _p, _p, _sz, _p]),
     "ptb_backward_events": (_st, [_p] * 8 + [_sz] + [_i64] * 4 + [_i32, _i32] + [_p] * 8
                             + [_sz, _p, _p, _i32]),
     "swa_attention_lse": (_st, [_p, _p, _p, _i64, _i32, _i64, _i32, _i32, ctypes.c_float, _p, _p,
@@ -324,6 +326,34 @@ def swa_attention_counts(q, k, v, window: int, scale: float = 0.0, stream=None):
                                   _ptr(o), _ptr(counts), _stream(stream))
     _check(st, "swa_attention_counts")
     return o, counts
+
+
+def host_workspace_size(batch: int, seq: int, hidden: int, ffn: int) -> int:
+    return int(load().ptb_forward_host_workspace_size(batch, seq, hidden, ffn))
+
+
+def ptb_forward_host(x_host, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, heads: int,
+                     window: int, y_host, workspace, stream=None):
+    """The layer on host-memory x and y (pinned CPU bf16 tensors) with device
+    parameters: enqueues H2D, the layer and D2H on the stream and returns
+    without waiting."""
+    lib = load()
+    for n, t in (("x_host", x_host), ("y_host", y_host)):
+        if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous host bf16 tensor")
+    if tuple(y_host.shape) != tuple(x_host.shape) or x_host.dim() != 3:
+        raise ValueError("x_host and y_host must be [batch, seq, hidden] of one shape")
+    for n, t in (("ln_gamma", ln_gamma), ("ln_beta", ln_beta), ("w_qkv", w_qkv), ("w_o", w_o),
+                 ("w_up", w_up), ("w_down", w_down)):
+        _bf16_cuda(n, t)
+    batch, seq, hidden = x_host.shape
+    ffn = w_up.shape[0]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.ptb_forward_host(_ptr(x_host), _ptr(ln_gamma), _ptr(ln_beta), _ptr(w_qkv), _ptr(w_o),
+                              _ptr(w_up), _ptr(w_down), batch, seq, hidden, ffn, heads, window,
+                              _ptr(y_host), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "ptb_forward_host")
+    return y_host
 
 
 def set_gemm_pairs(mode: int) -> int:

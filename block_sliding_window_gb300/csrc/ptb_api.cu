@@ -877,6 +877,41 @@ ptb_status ptb_forward(const ptb_bf16* x, const ptb_bf16* ln_gamma, const ptb_bf
                             ffn, heads, window, y, workspace, workspace_bytes, stream, nullptr, 0);
 }
 
+size_t ptb_forward_host_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn) {
+  const size_t layer = ptb_forward_workspace_size(batch, seq, hidden, ffn);
+  if (!layer) return 0;
+  const size_t t = static_cast<size_t>(batch) * static_cast<size_t>(seq);
+  return 2 * round_up(t * hidden * 2, kAlign) + layer;
+}
+
+ptb_status ptb_forward_host(const ptb_bf16* x_host, const ptb_bf16* ln_gamma,
+                            const ptb_bf16* ln_beta, const ptb_bf16* w_qkv, const ptb_bf16* w_o,
+                            const ptb_bf16* w_up, const ptb_bf16* w_down, int64_t batch,
+                            int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
+                            int32_t window, ptb_bf16* y_host, void* workspace,
+                            size_t workspace_bytes, ptb_stream stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (!x_host || !y_host || !workspace) return PTB_ERR_ARG;
+  const size_t need = ptb_forward_host_workspace_size(batch, seq, hidden, ffn);
+  if (!need) return PTB_ERR_ARG;
+  if (workspace_bytes < need) return PTB_ERR_WORKSPACE;
+  if (!aligned(workspace, kAlign)) return PTB_ERR_ALIGN;
+  const size_t bytes = static_cast<size_t>(batch) * seq * hidden * 2;
+  char* ws = static_cast<char*>(workspace);
+  ptb_bf16* x_dev = reinterpret_cast<ptb_bf16*>(ws);
+  ptb_bf16* y_dev = reinterpret_cast<ptb_bf16*>(ws + round_up(bytes, kAlign));
+  void* layer_ws = ws + 2 * round_up(bytes, kAlign);
+  const size_t layer_bytes = need - 2 * round_up(bytes, kAlign);
+  if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  ptb_status st = ptb_forward(x_dev, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, batch, seq,
+                              hidden, ffn, heads, window, y_dev, layer_ws, layer_bytes, stream_);
+  if (st != PTB_OK) return st;
+  if (cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  return PTB_OK;
+}
+
 ptb_status ptb_release_workspace(void) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PTB_ERR_DEVICE;

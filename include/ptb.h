@@ -118,6 +118,29 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
                               int32_t n_events);
 
 /*
+ * ptb_forward_host: ptb_forward with x and y in host memory (the layer's
+ * parameters stay in device memory).  Enqueues on `stream`: the copy of x
+ * [batch, seq, hidden] to the device, the layer, and the copy of y back;
+ * returns without waiting, so y_host is valid once the stream has reached
+ * that point (cudaStreamSynchronize or an event).  x_host and y_host should
+ * be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to run
+ * asynchronously and overlap with another stream's work; pageable memory
+ * works but the copies then block the calling thread.  `workspace` is
+ * caller-owned device memory of ptb_forward_host_workspace_size bytes
+ * (256-byte aligned; not null), holding the device copies of x and y and
+ * the layer's scratch; calls in flight at the same time need separate
+ * workspaces.  Errors as ptb_forward.
+ */
+size_t ptb_forward_host_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn);
+ptb_status ptb_forward_host(const ptb_bf16* x_host, const ptb_bf16* ln_gamma,
+                            const ptb_bf16* ln_beta, const ptb_bf16* w_qkv, const ptb_bf16* w_o,
+                            const ptb_bf16* w_up, const ptb_bf16* w_down, int64_t batch,
+                            int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
+                            int32_t window, ptb_bf16* y_host, void* workspace,
+                            size_t workspace_bytes, ptb_stream stream);
+
+/*
+ * ptb_forward_noalloc:/*
  * ptb_forward_noalloc: ptb_forward for callers that cannot allocate device
  * memory.  The paper has no counterpart; this is a deployment convenience.
  *

@@ -439,3 +439,25 @@ def test_ptb_forward_full_size_pairs_175b(ptb_lib, gemm_pairs):
     rel, mx, ex = errors(y[0, rows], want[0])
     print(f"175b pairs: rel-L2 {rel:.3e}, max-abs {mx:.3e}, beyond rounding {ex:.3e}")
     assert rel <= REL_L2 and ex <= max(MAX_ABS, 1.25 * floor)
+
+
+def test_forward_host_buffers_two_streams(ptb_lib):
+    """ptb_forward_host on pinned host x / y, two calls in flight on two
+    streams with their own workspaces: the same bits as ptb_forward."""
+    cfg = workloads.small_ptb(2, 300, 256, 4, 1024, 100, seed=43)
+    host = workloads.ptb_inputs(cfg)
+    d = _cuda(host)
+    w = (d["ln_gamma"], d["ln_beta"], d["w_qkv"], d["w_o"], d["w_up"], d["w_down"])
+    want = ptb_lib.ptb_forward(d["x"], *w, cfg.heads, cfg.window).cpu()
+    x2 = workloads.normal_bf16(tuple(host["x"].shape), seed=44)
+    want2 = ptb_lib.ptb_forward(x2.cuda(), *w, cfg.heads, cfg.window).cpu()
+    xs = [host["x"].pin_memory(), x2.pin_memory()]
+    ys = [torch.empty_like(xs[0]).pin_memory() for _ in range(2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    nbytes = ptb_lib.host_workspace_size(cfg.batch, cfg.seq, cfg.hidden, cfg.ffn)
+    wss = [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    for i in range(2):
+        ptb_lib.ptb_forward_host(xs[i], *w, cfg.heads, cfg.window, ys[i], wss[i],
+                                 stream=streams[i])
+    torch.cuda.synchronize()
+    assert torch.equal(ys[0], want) and torch.equal(ys[1], want2)
