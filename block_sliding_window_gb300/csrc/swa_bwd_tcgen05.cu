@@ -18,11 +18,14 @@
 //   kQ   one item = 128 queries: stationary Q and dO, moving 64-key tiles
 //          S = Q K^T,  dP = dO V^T            (M 128 queries, N 64, K d)
 //          dQ += dS K                         (M 128, N d, K 64 keys)
-// Roles (192 threads): warp 0 TMA, warp 1 TMEM owner and MMA issuer, warps
-// 2..5 one stationary row per thread (TMEM lane = row): recompute P and dS
-// for the tile in fp32, write them as bf16 operand rows into shared memory
-// (128-byte-swizzled K-major layout, two buffers), and at the end of an item
-// read the fp32 accumulators from TMEM and store bf16 gradients.  The
+// Roles (320 threads): warp 0 TMA, warp 1 TMEM owner and MMA issuer, warps
+// 2..9 two warpgroups; warp w serves the stationary rows of TMEM lane
+// quarter w % 4 (one row per thread) and the tile's columns 32 * g .. +31 of
+// its warpgroup g: recompute P and dS for them in fp32, write them as bf16
+// operand half-rows into shared memory (128-byte-swizzled K-major layout, one
+// buffer), and at the end of an item read the fp32 accumulators from TMEM
+// and store bf16 gradients.  (With one warpgroup doing all 64 columns the
+// kernels ran at 14-19% tensor activity, ~6k / 3.5k cycles per tile.)  The
 // moving tiles are read twice, once as K-major and once as MN-major operands
 // of the same shared-memory copy.
 // Every mbarrier wait is bounded (see mbar_wait); on a timeout all roles
@@ -34,7 +37,8 @@ namespace {
 
 constexpr int BR = 128;  // stationary rows per item (= MMA M)
 constexpr int BC = 64;   // moving rows per tile (= N of the score MMAs)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kGroupCols = BC / 2;  // moving columns per softmax warpgroup
 constexpr int kKV = 0;   // dK, dV kernel
 constexpr int kQ = 1;    // dQ kernel
 
@@ -43,12 +47,18 @@ struct BwdCfg {
   static constexpr int kAtoms = (D + 63) / 64;
   static constexpr int kStatBytes = kAtoms * BR * 128;  // one stationary operand
   static constexpr int kMvBytes = kAtoms * BC * 128;    // one moving operand, one stage
-  static constexpr int kNS = MODE == kKV ? 2 : 3;        // moving stages
+  // One operand buffer (the accumulate MMAs of a tile are short, so the
+  // rows of the next tile rarely wait for them) leaves room for more stages
+  // of moving tiles, which is what these latency-bound kernels need.
+  static constexpr int kOpBufs = 1;
   static constexpr int kOpRowBytes = BR * 128;          // one P / dS operand buffer
   static constexpr int kNOps = MODE == kKV ? 2 : 1;      // P^T and dS^T, or dS
-  static constexpr int kStageLse = 4 * 2 * BC * 4;       // per-warp lse / delta staging (kKV)
-  static constexpr int kSmemBytes = 2 * kStatBytes + kNS * 2 * kMvBytes +
-                                    2 * kNOps * kOpRowBytes + kStageLse + 512 + 1024;
+  static constexpr int kStageLse = 8 * 2 * kGroupCols * 4;  // per-warp lse / delta (kKV)
+  static constexpr int kFixed = 2 * kStatBytes + kOpBufs * kNOps * kOpRowBytes + kStageLse +
+                                512 + 1024;
+  static constexpr int kNSFit = (227 * 1024 - kFixed) / (2 * kMvBytes);
+  static constexpr int kNS = kNSFit < 6 ? kNSFit : 6;   // moving stages
+  static constexpr int kSmemBytes = kFixed + kNS * 2 * kMvBytes;
   static constexpr int kTmemCols = 512;
   // Score buffers: S at buf * 128, dP at buf * 128 + 64; accumulators after.
   __host__ __device__ static constexpr int s_col(int buf) { return buf * 128; }
@@ -130,14 +140,17 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float (
                    pack_bf16x2(v[e + 6] * mul, v[e + 7] * mul));
 }
 
-// One 64-value bf16 operand row (128 bytes) into row r of a 128-byte-swizzled
-// K-major tile: 16-byte chunk c sits at chunk position c ^ (r % 8).
-__device__ __forceinline__ void store_op_row(uint8_t* tile, int r, const uint32_t (&pk)[32]) {
+// 32 bf16 values (64 bytes: 16-byte chunks 4g .. 4g + 3 of the row) into row
+// r of a 128-byte-swizzled K-major tile.
+__device__ __forceinline__ void store_op_half(uint8_t* tile, int r, int g,
+                                              const uint32_t (&pk)[16]) {
   uint8_t* row = tile + r * 128;
 #pragma unroll
-  for (int c = 0; c < 8; ++c)
+  for (int j = 0; j < 4; ++j) {
+    const int c = 4 * g + j;
     *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
-        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+  }
 }
 
 template <int D, int MODE>
@@ -150,8 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sStat = smem;                               // [2][kStatBytes]
   uint8_t* sMv = sStat + 2 * C::kStatBytes;            // [NS][2][kMvBytes]
-  uint8_t* sOp = sMv + NS * 2 * C::kMvBytes;           // [2 buffers][kNOps][kOpRowBytes]
-  float* sLse = reinterpret_cast<float*>(sOp + 2 * C::kNOps * C::kOpRowBytes);  // [4][2][BC]
+  uint8_t* sOp = sMv + NS * 2 * C::kMvBytes;           // [kOpBufs][kNOps][kOpRowBytes]
+  float* sLse = reinterpret_cast<float*>(sOp + C::kOpBufs * C::kNOps * C::kOpRowBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sLse) + C::kStageLse);
   uint64_t* stat_full = bars;
   uint64_t* stat_empty = stat_full + 1;
@@ -178,11 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(&s_full[k], 1);
-      mbar_init(&p_full[k], 4);
+      mbar_init(&p_full[k], 8);
       mbar_init(&op_done[k], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
+    mbar_init(acc_empty, 8);
     mbar_init(done_bar, 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -297,8 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
             const uint32_t mc = mv_count + j - 1;
             const int st = mc % NS;
             const uint32_t mv0 = smem_addr(sMv + st * 2 * C::kMvBytes), mv1 = mv0 + C::kMvBytes;
-            const uint32_t n = op_issued;  // operand buffer n % 2
-            if (!mbar_wait(&p_full[n & 1], (n >> 1) & 1, abort_flag, a.status)) {
+            const uint32_t n = op_issued;  // operand buffer n % kOpBufs
+            const uint32_t ob = n % C::kOpBufs, oph = (n / C::kOpBufs) & 1;
+            if (!mbar_wait(&p_full[ob], oph, abort_flag, a.status)) {
               ok = false;
               break;
             }
@@ -309,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
               }
             }
             tc_fence_after();
-            const uint32_t op = smem_addr(sOp + (n & 1) * C::kNOps * C::kOpRowBytes);
+            const uint32_t op = smem_addr(sOp + ob * C::kNOps * C::kOpRowBytes);
             const bool first = j == 1;
             // The moving tile as the MN-major B operand: rows = its 64
             // positions (K), 64-column blocks of d (N) 64 * 128 bytes apart.
@@ -333,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
                              sw128_mnmajor_desc(mv0 + kk * 16 * 128, BC * 128), idesc_acc,
                              (!first || kk > 0) ? 1u : 0u);
             }
-            umma_commit(&op_done[n & 1]);
+            umma_commit(&op_done[ob]);
             umma_commit(&mv_empty[st]);
             ++op_issued;
           }
@@ -351,12 +365,14 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
     // ------------------------------------------------- P, dS and output --
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // stationary row = TMEM lane
+    const int grp = (warp - 2) >> 2;    // this warpgroup's columns: 32 * grp .. +31
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    float* wl = sLse + (warp - 2) * 2 * BC;  // this warp's lse / delta staging (kKV)
+    float* wl = sLse + (warp - 2) * 2 * kGroupCols;  // this warp's lse / delta staging (kKV)
     uint32_t seen = 0, items_done = 0;
     bool ok = true;
-    auto wait_op = [&](uint32_t n) -> bool {  // operand buffer n % 2 free again
-      if (!mbar_wait_warp(&op_done[n & 1], (n >> 1) & 1, abort_flag, a.status)) return false;
+    auto wait_op = [&](uint32_t n) -> bool {  // operand buffer n % kOpBufs free again
+      if (!mbar_wait_warp(&op_done[n % C::kOpBufs], (n / C::kOpBufs) & 1, abort_flag, a.status))
+        return false;
       tc_fence_after();
       return true;
     };
@@ -370,15 +386,14 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
         delta_row = a.delta[bh * a.seq + row];
       }
       for (int t = 0; t < it.n_tiles; ++t) {
-        const int c0 = (it.t_lo + t) * BC;  // first moving position of the tile
+        // First moving position of this warpgroup's 32 columns of the tile.
+        const int c0 = (it.t_lo + t) * BC + grp * kGroupCols;
         const int buf = seen & 1;
-        if (MODE == kKV) {  // per-query lse and delta of the tile, staged per warp
+        if (MODE == kKV) {  // per-query lse and delta of the columns, staged per warp
           __syncwarp();
-          for (int e = lane; e < BC; e += 32) {
-            const int q = c0 + e;
-            wl[e] = q < a.seq ? a.lse[bh * a.seq + q] : 0.f;
-            wl[BC + e] = q < a.seq ? a.delta[bh * a.seq + q] : 0.f;
-          }
+          const int q = c0 + lane;
+          wl[lane] = q < a.seq ? a.lse[bh * a.seq + q] : 0.f;
+          wl[kGroupCols + lane] = q < a.seq ? a.delta[bh * a.seq + q] : 0.f;
           __syncwarp();
         }
         if (!mbar_wait_warp(&s_full[buf], (seen >> 1) & 1, abort_flag, a.status)) {
@@ -386,22 +401,19 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
           break;
         }
         tc_fence_after();
-        float s[BC], dp[BC];
+        uint32_t s_raw[kGroupCols], dp_raw[kGroupCols];
+        tmem_ld_32x32b_x32(tmem + lane_base + C::s_col(buf) + grp * kGroupCols, s_raw);
+        tmem_ld_32x32b_x32(tmem + lane_base + C::dp_col(buf) + grp * kGroupCols, dp_raw);
+        tmem_ld_wait();
+        float s[kGroupCols], dp[kGroupCols];
 #pragma unroll
-        for (int c = 0; c < BC; c += 32) {
-          uint32_t raw[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + C::s_col(buf) + c, raw);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[c + e] = __uint_as_float(raw[e]);
-          tmem_ld_32x32b_x32(tmem + lane_base + C::dp_col(buf) + c, raw);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) dp[c + e] = __uint_as_float(raw[e]);
+        for (int e = 0; e < kGroupCols; ++e) {
+          s[e] = __uint_as_float(s_raw[e]);
+          dp[e] = __uint_as_float(dp_raw[e]);
         }
-        uint32_t pk_p[BC / 2], pk_ds[BC / 2];
+        uint32_t pk_p[kGroupCols / 2], pk_ds[kGroupCols / 2];
 #pragma unroll
-        for (int e = 0; e < BC; e += 2) {
+        for (int e = 0; e < kGroupCols; e += 2) {
           float pv[2], dsv[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
@@ -411,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
             const int kj = MODE == kKV ? row : c;
             const bool vis = kj <= qi && qi - kj < a.window && qi < a.seq && kj < a.seq;
             const float l2 = MODE == kKV ? wl[e + u] : lse_row;
-            const float dl = MODE == kKV ? wl[BC + e + u] : delta_row;
+            const float dl = MODE == kKV ? wl[kGroupCols + e + u] : delta_row;
             const float p = vis ? fast_exp2(s[e + u] * a.scale_log2 - l2) : 0.f;
             pv[u] = p;
             dsv[u] = p * (dp[e + u] - dl);
@@ -419,22 +431,24 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
           pk_p[e / 2] = pack_bf16x2(pv[0], pv[1]);
           pk_ds[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
         }
-        // Operand buffer `buf` was last read by the accumulate MMAs seen - 2.
-        if (seen >= 2 && !wait_op(seen - 2)) {
+        // The operand buffer was last read by the accumulate MMAs of tile
+        // seen - kOpBufs.
+        if (seen >= static_cast<uint32_t>(C::kOpBufs) && !wait_op(seen - C::kOpBufs)) {
           ok = false;
           break;
         }
-        uint8_t* ops = sOp + buf * C::kNOps * C::kOpRowBytes;
+        const int ob = static_cast<int>(seen % C::kOpBufs);
+        uint8_t* ops = sOp + ob * C::kNOps * C::kOpRowBytes;
         if constexpr (MODE == kKV) {
-          store_op_row(ops, r, pk_p);
-          store_op_row(ops + C::kOpRowBytes, r, pk_ds);
+          store_op_half(ops, r, grp, pk_p);
+          store_op_half(ops + C::kOpRowBytes, r, grp, pk_ds);
         } else {
-          store_op_row(ops, r, pk_ds);
+          store_op_half(ops, r, grp, pk_ds);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[buf]);
+        if (lane == 0) mbar_arrive(&p_full[ob]);
         ++seen;
       }
       if (!ok) break;
@@ -446,13 +460,16 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
       tc_fence_after();
       const int prow = row < a.seq ? row : 0;
       float g[D];
-      if constexpr (MODE == kKV) {
-        tmem_row<D>(tmem + lane_base + C::acc_col(0), g);
-        if (row < a.seq) store_row_bf16<D>(a.dv + it.b * a.dv_sb + it.h * a.dv_sh + prow * a.dv_ss, g, 1.f);
-        tmem_row<D>(tmem + lane_base + C::acc_col(1), g);
-        if (row < a.seq)
-          store_row_bf16<D>(a.dk + it.b * a.dk_sb + it.h * a.dk_sh + prow * a.dk_ss, g, a.scale);
-      } else {
+      if constexpr (MODE == kKV) {  // warpgroup 0: dV, warpgroup 1: dK
+        tmem_row<D>(tmem + lane_base + C::acc_col(grp), g);
+        if (row < a.seq) {
+          if (grp == 0)
+            store_row_bf16<D>(a.dv + it.b * a.dv_sb + it.h * a.dv_sh + prow * a.dv_ss, g, 1.f);
+          else
+            store_row_bf16<D>(a.dk + it.b * a.dk_sb + it.h * a.dk_sh + prow * a.dk_ss, g,
+                              a.scale);
+        }
+      } else if (grp == 0) {
         tmem_row<D>(tmem + lane_base + C::acc_col(0), g);
         if (row < a.seq)
           store_row_bf16<D>(a.dq + it.b * a.dq_sb + it.h * a.dq_sh + prow * a.dq_ss, g, a.scale);
