@@ -525,12 +525,13 @@ struct PairCfg {
   static constexpr int kSmemBytes = kPairStages * kStageBytes + kBarBytes + 1024;
 };
 
-template <int EPI, int LAYOUT>
+template <int EPI, int LAYOUT, bool FP8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ GemmArgs p) {
   using C = PairCfg;
   constexpr int BN = kPairBN;
-  constexpr int BK = 64;
+  constexpr int BK = Elem<FP8>::kBK;
+  static_assert(!(FP8 && LAYOUT != kLayoutKK), "e4m3 operands are K-major only");
   constexpr int NS = kPairStages;
   // MN-major operands arrive as 64-wide MN blocks of 64 K rows (8 KB each).
   constexpr bool kAmn = (LAYOUT & 1) != 0;
@@ -660,8 +661,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ----------------------------------------------------- MMA issuer --
-      constexpr uint32_t idesc = umma_idesc_bf16(2 * BM, BN) | (kAmn ? 1u << 15 : 0u) |
-                                 (kBmn ? 1u << 16 : 0u);
+      constexpr uint32_t idesc =
+          (FP8 ? umma_idesc_e4m3(2 * BM, BN) : umma_idesc_bf16(2 * BM, BN)) |
+          (kAmn ? 1u << 15 : 0u) | (kBmn ? 1u << 16 : 0u);
       constexpr uint64_t kStepA = kAmn ? 128 : 2;
       constexpr uint64_t kStepB = kBmn ? 128 : 2;
       int stage = 0;
@@ -685,9 +687,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint64_t bdesc = kBmn ? sw128_mnmajor_desc(smem_addr(stage_b(stage)), kMnBlock)
                                       : sw128_kmajor_desc(smem_addr(stage_b(stage)));
 #pragma unroll
-          for (int kk = 0; kk < kMmasPerBlock; ++kk)
-            umma_bf16_pair(d_tmem, adesc + kStepA * kk, bdesc + kStepB * kk, idesc,
-                           (kb != u.kb0 || kk != 0) ? 1u : 0u);
+          for (int kk = 0; kk < kMmasPerBlock; ++kk) {
+            const uint32_t accum = (kb != u.kb0 || kk != 0) ? 1u : 0u;
+            if constexpr (FP8)
+              umma_e4m3_pair(d_tmem, adesc + kStepA * kk, bdesc + kStepB * kk, idesc, accum);
+            else
+              umma_bf16_pair(d_tmem, adesc + kStepA * kk, bdesc + kStepB * kk, idesc, accum);
+          }
           umma_commit_pair(&empty_bar[stage], 0x3);
           if (++stage == NS) {
             stage = 0;
@@ -722,7 +728,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int prow = static_cast<int>(rank) * BM + row_local;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc_buf * BN);
-      epilogue_unit<BN, EPI, false, 2 * BM>(
+      epilogue_unit<BN, EPI, FP8, 2 * BM>(
           p, u, m0 + prow, prow, (u.slot / p.split_s) * 8 + static_cast<int>(rank) * 4 + quarter,
           t_row, n0, lane);
       tc_fence_before();
@@ -741,10 +747,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int EPI, int LAYOUT>
+template <int EPI, int LAYOUT, bool FP8 = false>
 cudaError_t launch_pair(const GemmArgs& a, cudaStream_t stream) {
   using C = PairCfg;
-  auto kern = gemm_pair_kernel<EPI, LAYOUT>;
+  auto kern = gemm_pair_kernel<EPI, LAYOUT, FP8>;
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -820,8 +826,14 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
         cudaMemsetAsync(a.counters, 0, a.split_r * (a.pair ? 8 : 4) * sizeof(unsigned), stream);
     if (e != cudaSuccess) return e;
   }
-  if (a.pair) {  // bf16, 256-wide N tiles on CTA pairs
-    if (a.fp8 || a.block_n != kPairBN) return cudaErrorInvalidValue;
+  if (a.pair) {  // 256-wide N tiles on CTA pairs
+    if (a.block_n != kPairBN) return cudaErrorInvalidValue;
+    if (a.fp8) {
+      if (a.layout != kLayoutKK) return cudaErrorInvalidValue;
+      if (a.epilogue == kEpiQkvGelu) return launch_pair<kEpiQkvGelu, kLayoutKK, true>(a, stream);
+      if (a.epilogue == kEpiResidual) return launch_pair<kEpiResidual, kLayoutKK, true>(a, stream);
+      return cudaErrorInvalidValue;
+    }
     if (a.layout == kLayoutKK && a.epilogue == kEpiQkvGelu)
       return launch_pair<kEpiQkvGelu, kLayoutKK>(a, stream);
     if (a.layout == kLayoutKK && a.epilogue == kEpiResidual)

@@ -120,7 +120,9 @@ size_t gemm_scratch_bytes(const GemmPlan& g) {
 // back 175B- and 530B-class forward layers (2.2e12 / 1.5e12 and 6.9e12 /
 // 5.2e12) run at the 1.4 kW power cap, where pairs ran their GEMMs no
 // faster, at 1500 instead of 1920 MHz, which then also slowed the attention
-// and LayerNorm kernels: the forward layer took 0.4-1.2% longer.
+// and LayerNorm kernels: the forward layer took 0.4-1.2% longer.  The e4m3
+// layer behaves alike: pairs took 5% off the 13B-class layer, nothing at 175B
+// (its GEMM holds 3.1 PFLOP/s at 2070 MHz either way) and added 3% at 530B.
 bool use_pairs(const DeviceState* ds, bool shape_ok, int64_t m, int64_t n, int64_t k,
                bool training) {
   if (!shape_ok || m <= 128 || ds->sms < 2 || ds->pairs == 0) return false;
@@ -221,7 +223,7 @@ ptb_status gemm_run(DeviceState* ds, const GemmSpec& g, int64_t tokens, ptb_bf16
   const int64_t K = g.k(), N = g.n();
   // CTA pairs for bf16 GEMMs with 256-wide N tiles and more than one
   // 128-row tile of M; each CTA of a pair loads half of the B tile.
-  a.pair = use_pairs(ds, !g.fp8 && a.block_n == 256, tokens, N, K, training) ? 1 : 0;
+  a.pair = use_pairs(ds, a.block_n == 256, tokens, N, K, training) ? 1 : 0;
   const uint32_t box_b = a.pair ? a.block_n / 2 : a.block_n;
   bool ok;
   if (g.k1) {
