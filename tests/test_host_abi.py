@@ -159,3 +159,37 @@ def test_product_package_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", text, flags=re.M), f
                 assert "oracle/" not in text, f
+
+
+def test_set_gemm_pairs_rejects_unknown_modes(lib):
+    import block_sliding_window_gb300 as bsw
+    for mode in (-2, 2, 7):
+        assert bsw.STATUS_NAMES[lib.ptb_set_gemm_pairs(mode, None)] == "PTB_ERR_ARG"
+
+
+def test_forward_host_argument_checks(lib):
+    import block_sliding_window_gb300 as bsw
+    ws = lib.ptb_forward_host_workspace_size(1, 128, 256, 1024)
+    assert ws >= 2 * 128 * 256 * 2 + lib.ptb_forward_workspace_size(1, 128, 256, 1024)
+    # null host buffers / workspace, and a workspace that is too small
+    st = lib.ptb_forward_host(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 1024, 4, 32,
+                              FAKE, FAKE, ws, None)
+    assert bsw.STATUS_NAMES[st] == "PTB_ERR_ARG"
+    st = lib.ptb_forward_host(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 1024, 4, 32,
+                              FAKE, None, ws, None)
+    assert bsw.STATUS_NAMES[st] == "PTB_ERR_ARG"
+    st = lib.ptb_forward_host(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 256, 1024, 4, 32,
+                              FAKE, FAKE, ws - 1, None)
+    assert bsw.STATUS_NAMES[st] == "PTB_ERR_WORKSPACE"
+
+
+def test_training_sizes(lib):
+    b, s, h, f, heads = 2, 300, 256, 1024, 4
+    t = b * s
+    saved = lib.ptb_train_saved_size(b, s, h, f, heads)
+    # xn, U, Z, ctx (bf16), LN stats and lse (fp32): each region rounded to 256 bytes
+    assert saved >= 2 * t * (h + 3 * h + f + f + h) + 8 * t + 4 * b * heads * s
+    ws = lib.ptb_backward_workspace_size(b, s, h, f, heads)
+    assert ws >= 2 * t * (h + 3 * h + f) + 4 * t * h
+    assert lib.ptb_train_saved_size(0, s, h, f, heads) == 0
+    assert lib.ptb_backward_workspace_size(b, s, 100, f, heads) == 0
