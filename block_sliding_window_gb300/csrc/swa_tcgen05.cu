@@ -11,8 +11,9 @@
 // every K/V tile.  320 threads:
 //   warp 0      TMA: the two Q tiles of an item, then the 64-key K and V
 //               tiles intersecting the item's band [q0 - w + 1, q0 + 255]
-//               (diagonal tile first) into a 3-stage ring that runs on
-//               across items.  d < 128 is read as 64-wide boxes; columns
+//               (diagonal tile first) into a ring of 4 stages (d > 64; 6 for
+//               d <= 64) that runs on across items.  d < 128 is read as
+//               64-wide boxes; columns
 //               past d are zero-filled by TMA.  (An L2 prefetch of the tiles
 //               four positions ahead was measured slightly slower.)
 //   warp 1      owns TMEM (512 columns: per query tile two 64-column score
@@ -27,9 +28,9 @@
 //               against a reference max that is raised only when the row max
 //               exceeds it by more than 8 (so P <= 2^8 in bf16); raising it
 //               rescales the running sum and the output row in TMEM.  The
-//               bf16 P row goes to shared memory (two buffers per query tile)
-//               in the 128-byte-swizzled operand layout, so a softmax warp
-//               never waits for a P V except to reuse a buffer two tiles old
+//               bf16 P row goes to shared memory (one buffer per query tile)
+//               in the 128-byte-swizzled operand layout; a softmax warp waits
+//               for a P V only to reuse the buffer (the previous tile's P V)
 //               or to rescale O.  At the end of an item O / l -> bf16.
 // Every mbarrier wait is bounded (see mbar_wait); on a timeout all roles
 // unwind, wait for their own copies and MMAs, free TMEM and return.
@@ -41,7 +42,6 @@ namespace {
 constexpr int BQ = 128;       // rows per query tile (= MMA M)
 constexpr int QT = 2;         // query tiles per work item
 constexpr int BKV = 64;       // keys per K/V tile (= MMA N of S, K of PV)
-constexpr int NS = 3;         // K/V stages
 constexpr int kThreads = 320;
 constexpr float kRescaleLog2 = 8.0f;  // raise the reference max only past 2^8
 
@@ -51,8 +51,13 @@ struct SwaCfg {
   static constexpr int kQTileBytes = kAtoms * BQ * 128;
   static constexpr int kKVBytes = kAtoms * BKV * 128;   // one of K or V, one stage
   static constexpr int kPBytes = BQ * BKV * 2;          // P of one query tile
-  static constexpr int kSmemBytes =
-      QT * kQTileBytes + NS * 2 * kKVBytes + QT * 2 * kPBytes + 512 + 1024;
+  // One P buffer per query tile (a P V is short, so the next tile's P rarely
+  // waits for it) leaves room for a deeper K/V ring.
+  static constexpr int kPBufs = 1;
+  static constexpr int kFixed = QT * kQTileBytes + QT * kPBufs * kPBytes + 512 + 1024;
+  static constexpr int kNSFit = (227 * 1024 - kFixed) / (2 * kKVBytes);
+  static constexpr int kNS = kNSFit < 6 ? kNSFit : 6;  // K/V stages
+  static constexpr int kSmemBytes = kFixed + kNS * 2 * kKVBytes;
   static constexpr int kTmemCols = 512;
   __host__ __device__ static constexpr int s_col(int x, int buf) { return x * 256 + buf * BKV; }
   __host__ __device__ static constexpr int o_col(int x) { return x * 256 + 2 * BKV; }
@@ -106,6 +111,8 @@ __device__ __forceinline__ bool tile_relevant(const SwaParams& P, const Item& it
 template <int D, bool COUNTS>
 __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_constant__ SwaParams P) {
   using C = SwaCfg<D>;
+  constexpr int NS = C::kNS;
+  constexpr int PB = C::kPBufs;
   const SwaArgs& a = P.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -113,16 +120,16 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
   uint8_t* sQ = smem;                               // [QT][kQTileBytes]
   uint8_t* sK = sQ + QT * C::kQTileBytes;           // [NS][kKVBytes]
   uint8_t* sV = sK + NS * C::kKVBytes;              // [NS][kKVBytes]
-  uint8_t* sP = sV + NS * C::kKVBytes;              // [QT][2][kPBytes]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + QT * 2 * C::kPBytes);
+  uint8_t* sP = sV + NS * C::kKVBytes;              // [QT][PB][kPBytes]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + QT * PB * C::kPBytes);
   uint64_t* q_full = bars;
   uint64_t* q_empty = q_full + 1;
   uint64_t* kv_full = q_empty + 1;      // [NS]
   uint64_t* kv_empty = kv_full + NS;    // [NS]
   uint64_t* s_full = kv_empty + NS;     // [QT][2]
-  uint64_t* p_full = s_full + 2 * QT;   // [QT][2]
-  uint64_t* pv_done = p_full + 2 * QT;  // [QT][2]
-  uint64_t* done_bar = pv_done + 2 * QT;
+  uint64_t* p_full = s_full + 2 * QT;   // [QT][PB]
+  uint64_t* pv_done = p_full + PB * QT; // [QT][PB]
+  uint64_t* done_bar = pv_done + PB * QT;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -139,9 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
     for (int x = 0; x < QT; ++x) {
       mbar_init(&s_full[2 * x], 1);
       mbar_init(&s_full[2 * x + 1], 1);
-      for (int k = 0; k < 2; ++k) {
-        mbar_init(&p_full[2 * x + k], 4);
-        mbar_init(&pv_done[2 * x + k], 1);
+      for (int k = 0; k < PB; ++k) {
+        mbar_init(&p_full[PB * x + k], 4);
+        mbar_init(&pv_done[PB * x + k], 1);
       }
     }
     mbar_init(done_bar, 1);
@@ -259,20 +266,21 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
             const uint32_t v_addr = smem_addr(sV + st * C::kKVBytes);
             for (int x = 0; x < QT; ++x) {
               if (!tile_relevant(P, it, x, key0)) continue;
-              const uint32_t n = pv_issued[x];  // P V number n uses P buffer n % 2
-              if (!mbar_wait(&p_full[2 * x + (n & 1)], (n >> 1) & 1, abort_flag, a.status)) {
+              const uint32_t n = pv_issued[x];  // P V number n uses P buffer n % PB
+              const uint32_t pb = PB * x + n % PB, pph = (n / PB) & 1;
+              if (!mbar_wait(&p_full[pb], pph, abort_flag, a.status)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              const uint32_t p_addr = smem_addr(sP + (2 * x + (n & 1)) * C::kPBytes);
+              const uint32_t p_addr = smem_addr(sP + pb * C::kPBytes);
               const uint32_t d_tmem = tmem + C::o_col(x);
 #pragma unroll
               for (int kk = 0; kk < BKV / 16; ++kk)
                 umma_bf16_ss(d_tmem, sw128_kmajor_desc(p_addr + kk * 32),
                              sw128_mnmajor_desc(v_addr + kk * 16 * 128, BKV * 128), idesc_pv,
                              (!first_pv[x] || kk > 0) ? 1u : 0u);
-              umma_commit(&pv_done[2 * x + (n & 1)]);
+              umma_commit(&pv_done[pb]);
               ++pv_issued[x];
               first_pv[x] = false;
             }
@@ -296,11 +304,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
     uint32_t seen = 0;  // relevant tiles of this query tile so far (all items)
     bool ok = true;
 
-    // P V number n of this query tile is signalled on pv_done[x][n % 2];
-    // waits never lag a barrier by two phases (P V n + 2 needs P n + 2,
+    // P V number n of this query tile is signalled on pv_done[x][n % PB];
+    // waits never lag a barrier by two phases (P V n + PB needs P n + PB,
     // which is only written after this wait).
     auto wait_pv = [&](uint32_t n) -> bool {
-      if (!mbar_wait_warp(&pv_done[2 * x + (n & 1)], (n >> 1) & 1, abort_flag, a.status))
+      if (!mbar_wait_warp(&pv_done[PB * x + n % PB], (n / PB) & 1, abort_flag, a.status))
         return false;
       tc_fence_after();
       return true;
@@ -365,12 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
           pk[e / 2] = pack_bf16x2(p0, p1);
         }
         l_run += rs;
-        // P buffer `buf` was last read by P V number seen - 2.
-        if (seen >= 2 && !wait_pv(seen - 2)) {
+        // The P buffer was last read by P V number seen - PB.
+        if (seen >= static_cast<uint32_t>(PB) && !wait_pv(seen - PB)) {
           ok = false;
           break;
         }
-        uint8_t* prow = sP + (2 * x + buf) * C::kPBytes + r * 128;
+        uint8_t* prow = sP + (PB * x + seen % PB) * C::kPBytes + r * 128;
         // Row r of P: 64 keys = one 128-byte swizzled row; 16-byte chunk c
         // sits at chunk position c ^ (r % 8).
 #pragma unroll
@@ -406,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[2 * x + buf]);
+        if (lane == 0) mbar_arrive(&p_full[PB * x + seen % PB]);
         any_pv = true;
         ++seen;
       }
