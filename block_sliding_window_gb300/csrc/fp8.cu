@@ -8,7 +8,7 @@
 //   * layernorm_fp8_kernel: xn = LN(x) quantized per token row.
 //   * quantize_rows_kernel: rows of [src0 | src1] (two column blocks of
 //     bf16 matrices) quantized per row -- the second GEMM's A operand
-//     [ctx | G] every layer, and the weights once.
+//     [ctx | G] every layer, and the weights once.  Two passes, no staging.
 // A row's scale is amax(|row|) / 448 (448 = largest finite e4m3), 1 for an
 // all-zero row; values are rounded to nearest e4m3 with saturation.
 #include <cuda_fp8.h>
@@ -126,32 +126,52 @@ __global__ void __launch_bounds__(kQThreads) layernorm_fp8_kernel(
 }
 
 // Row r of the output is [src0[r, 0:n0] | src1[r, 0:n1]] quantized with one
-// scale; written to out[(row0 + r) * (n0 + n1) ...] and scale[row0 + r].  The
-// row is staged in shared memory between the amax pass and the store.
+// scale; written to out[(row0 + r) * (n0 + n1) ...] and scale[row0 + r].
+// Two passes over the row: the amax, then (re-reading the row, mostly from
+// L2) the quantized store.  Nothing is staged in shared memory, so eight
+// CTAs fit on an SM and the loads of one row overlap those of others.  (A
+// version that staged the row in shared memory ran one CTA per SM and took
+// 122 us for the 175B-shaped [ctx | G], 2048 x 61440.)
+__device__ __forceinline__ uint4 row_vec(const uint4* a, const uint4* b, int v0, int i) {
+  return i < v0 ? __ldg(a + i) : __ldg(b + (i - v0));
+}
+
 __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
     const __nv_bfloat16* __restrict__ src0, int64_t ld0, int n0,
     const __nv_bfloat16* __restrict__ src1, int64_t ld1, int n1, int64_t row0,
     uint8_t* __restrict__ out, float* __restrict__ scale) {
-  extern __shared__ uint4 qrow[];
   __shared__ float red[kQThreads / 32];
   const int64_t r = blockIdx.x;
-  const int v0 = n0 / 8, v1 = n1 / 8;
+  const int v0 = n0 / 8, nv = (n0 + n1) / 8;
   const uint4* a = reinterpret_cast<const uint4*>(src0 + r * ld0);
-  const uint4* b = src1 ? reinterpret_cast<const uint4*>(src1 + r * ld1) : nullptr;
+  const uint4* b = src1 ? reinterpret_cast<const uint4*>(src1 + r * ld1) : a;
   float amax = 0.f;
-  for (int i = threadIdx.x; i < v0 + v1; i += kQThreads) {
-    const uint4 c = i < v0 ? __ldg(a + i) : __ldg(b + (i - v0));
-    qrow[i] = c;
+  int i = threadIdx.x;
+  for (; i + 3 * kQThreads < nv; i += 4 * kQThreads) {  // four 16-byte loads in flight
+    uint4 c[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) c[u] = row_vec(a, b, v0, i + u * kQThreads);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t w[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
+    }
+  }
+  for (; i < nv; i += kQThreads) {
+    const uint4 c = row_vec(a, b, v0, i);
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
+    for (int e = 0; e < 4; ++e)
+      amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
   }
-  amax = block_reduce(amax, red, true);  // also orders the qrow writes before the reads
+  amax = block_reduce(amax, red, true);
   const float s = amax > 0.f ? amax / kE4m3Max : 1.f;
   const float inv = 1.f / s;
   uint2* dst = reinterpret_cast<uint2*>(out + (row0 + r) * static_cast<int64_t>(n0 + n1));
-  for (int i = threadIdx.x; i < v0 + v1; i += kQThreads) {
-    const uint4 c = qrow[i];
+  for (int j = threadIdx.x; j < nv; j += kQThreads) {
+    const uint4 c = row_vec(a, b, v0, j);
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
     float f[8];
 #pragma unroll
@@ -159,7 +179,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
       f[2 * e] = bf16_lo(w[e]);
       f[2 * e + 1] = bf16_hi(w[e]);
     }
-    dst[i] = quant8(f, inv);
+    dst[j] = quant8(f, inv);
   }
   if (threadIdx.x == 0) scale[row0 + r] = s;
 }
@@ -181,27 +201,9 @@ cudaError_t launch_layernorm_fp8(const __nv_bfloat16* x, const __nv_bfloat16* ga
 cudaError_t launch_quantize_rows(const __nv_bfloat16* src0, int64_t ld0, int n0,
                                  const __nv_bfloat16* src1, int64_t ld1, int n1, int64_t rows,
                                  int64_t row0, uint8_t* out, float* scale, cudaStream_t stream) {
-  // The opt-in limit (227 KB per block) covers the static reduction array too.
-  static int configured_device = -1;
-  static size_t max_dynamic = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    cudaFuncAttributes fa{};
-    e = cudaFuncGetAttributes(&fa, quantize_rows_kernel);
-    if (e != cudaSuccess) return e;
-    const size_t limit = 227 * 1024 - fa.sharedSizeBytes;
-    e = cudaFuncSetAttribute(quantize_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(limit));
-    if (e != cudaSuccess) return e;
-    max_dynamic = limit;
-    configured_device = dev;
-  }
-  const size_t smem = static_cast<size_t>(n0 + n1) * 2;
-  if (n0 % 8 || n1 % 8 || smem > max_dynamic || rows > 0x7fffffff) return cudaErrorInvalidValue;
+  if (n0 % 8 || n1 % 8 || n0 + n1 <= 0 || rows > 0x7fffffff) return cudaErrorInvalidValue;
   if (rows <= 0) return cudaSuccess;
-  quantize_rows_kernel<<<static_cast<unsigned>(rows), kQThreads, smem, stream>>>(
+  quantize_rows_kernel<<<static_cast<unsigned>(rows), kQThreads, 0, stream>>>(
       src0, ld0, n0, src1, ld1, n1, row0, out, scale);
   return cudaGetLastError();
 }

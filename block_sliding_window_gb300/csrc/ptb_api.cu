@@ -1080,7 +1080,7 @@ ptb_status ptb_prepare_fp8_weights(const ptb_bf16* w_qkv, const ptb_bf16* w_o,
   for (const void* p : ptrs)
     if (!aligned(p, 16)) return PTB_ERR_ALIGN;
   if (hidden < 128 || ffn < 128) return PTB_ERR_ARG;
-  if (hidden % 128 || ffn % 128 || (hidden + ffn) * 2 > kQuantizeRowMaxBytes) return PTB_ERR_SHAPE;
+  if (hidden % 128 || ffn % 128) return PTB_ERR_SHAPE;
   DeviceState* ds = nullptr;
   ptb_status st = device_state(&ds);
   if (st != PTB_OK) return st;
@@ -1106,8 +1106,8 @@ ptb_status ptb_forward_fp8_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
   const void* ptrs[] = {x, ln_gamma, ln_beta, w1, s1, w2, s2, y};
   ptb_status st = check_layer(ptrs, 8, batch, seq, hidden, ffn, heads, window);
   if (st != PTB_OK) return st;
-  // e4m3 k-blocks are 128 elements; a quantized row is staged in shared memory.
-  if (hidden % 128 || ffn % 128 || (hidden + ffn) * 2 > kQuantizeRowMaxBytes) return PTB_ERR_SHAPE;
+  // e4m3 k-blocks are 128 elements.
+  if (hidden % 128 || ffn % 128) return PTB_ERR_SHAPE;
   if (events && n_events != 6) return PTB_ERR_ARG;
   if (events)
     for (int i = 0; i < 6; ++i)

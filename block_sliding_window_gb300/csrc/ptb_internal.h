@@ -77,9 +77,6 @@ struct GemmArgs {
 
 // Each K piece of a split tile keeps at least this many 64-wide k-blocks.
 constexpr int kMinSplitKBlocks = 8;
-// Largest bf16 row (bytes) the e4m3 row quantizer stages in shared memory:
-// the 227 KB opt-in block limit less room for its static reduction array.
-constexpr int64_t kQuantizeRowMaxBytes = 226 * 1024;
 
 struct GemmPlan {
   int grid, split_r, split_s;

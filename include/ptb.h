@@ -207,7 +207,7 @@ ptb_status ptb_serial_forward(const ptb_bf16* x, const ptb_bf16* ln1_gamma,
  * tests bound it by an exact computation with the same e4m3 rounding points.
  *
  * ptb_prepare_fp8_weights quantizes the bf16 weights once (w1, s1, w2, s2 are
- * caller-owned device buffers of the sizes above; (H + F) * 2 <= 226 KiB).
+ * caller-owned device buffers of the sizes above).
  * ptb_forward_fp8 then runs LN+quantize, the e4m3 [QKV | up] GEMM + GELU,
  * SWA, a row quantization of [ctx | G], and the e4m3 [out | down] GEMM + x.
  * Same shape rules, workspace and error conventions as ptb_forward, except
