@@ -50,6 +50,9 @@ __device__ __forceinline__ uint2 quant8(const float (&v)[8], float inv) {
   return make_uint2(lo, hi);
 }
 
+// VPT: 16-byte vectors of the row per thread (the row cache is sized to the
+// hidden size so that more CTAs fit on an SM).
+template <int VPT>
 __global__ void __launch_bounds__(kQThreads) layernorm_fp8_kernel(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
     const __nv_bfloat16* __restrict__ beta, int hidden, float eps, uint8_t* __restrict__ out,
@@ -60,10 +63,10 @@ __global__ void __launch_bounds__(kQThreads) layernorm_fp8_kernel(
   const uint4* src = reinterpret_cast<const uint4*>(x + row * hidden);
   const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
   const uint4* b4 = reinterpret_cast<const uint4*>(beta);
-  uint4 cache[kLnMaxVec];
+  uint4 cache[VPT];
   float sum = 0.f;
 #pragma unroll
-  for (int j = 0; j < kLnMaxVec; ++j) {
+  for (int j = 0; j < VPT; ++j) {
     const int i = threadIdx.x + j * kQThreads;
     if (i < nvec) {
       cache[j] = __ldcs(src + i);
@@ -75,7 +78,7 @@ __global__ void __launch_bounds__(kQThreads) layernorm_fp8_kernel(
   const float mean = block_reduce(sum, red, false) / static_cast<float>(hidden);
   float sq = 0.f;
 #pragma unroll
-  for (int j = 0; j < kLnMaxVec; ++j) {
+  for (int j = 0; j < VPT; ++j) {
     if (threadIdx.x + j * kQThreads < nvec) {
       const uint32_t w[4] = {cache[j].x, cache[j].y, cache[j].z, cache[j].w};
 #pragma unroll
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(kQThreads) layernorm_fp8_kernel(
   };
   float amax = 0.f;
 #pragma unroll
-  for (int j = 0; j < kLnMaxVec; ++j) {
+  for (int j = 0; j < VPT; ++j) {
     const int i = threadIdx.x + j * kQThreads;
     if (i < nvec) {
       float f[8];
@@ -114,7 +117,7 @@ __global__ void __launch_bounds__(kQThreads) layernorm_fp8_kernel(
   const float inv = 1.f / s;
   uint2* dst = reinterpret_cast<uint2*>(out + row * hidden);
 #pragma unroll
-  for (int j = 0; j < kLnMaxVec; ++j) {
+  for (int j = 0; j < VPT; ++j) {
     const int i = threadIdx.x + j * kQThreads;
     if (i < nvec) {
       float f[8];
@@ -192,10 +195,25 @@ cudaError_t launch_layernorm_fp8(const __nv_bfloat16* x, const __nv_bfloat16* ga
   if (hidden % 8 != 0 || hidden / 8 > kLnMaxVec * kQThreads || rows > 0x7fffffff)
     return cudaErrorInvalidValue;
   if (rows <= 0) return cudaSuccess;
-  layernorm_fp8_kernel<<<static_cast<unsigned>(rows), kQThreads, 0, stream>>>(x, gamma, beta,
-                                                                             hidden, eps, out,
-                                                                             scale);
-  return cudaGetLastError();
+  const int vpt = (hidden / 8 + kQThreads - 1) / kQThreads;
+  const unsigned grid = static_cast<unsigned>(rows);
+#define PTB_LNQ_CASE(V)                                                                        \
+  if (vpt <= V) {                                                                               \
+    layernorm_fp8_kernel<V><<<grid, kQThreads, 0, stream>>>(x, gamma, beta, hidden, eps, out,  \
+                                                            scale);                            \
+    return cudaGetLastError();                                                                  \
+  }
+  PTB_LNQ_CASE(1)
+  PTB_LNQ_CASE(2)
+  PTB_LNQ_CASE(3)
+  PTB_LNQ_CASE(4)
+  PTB_LNQ_CASE(6)
+  PTB_LNQ_CASE(8)
+  PTB_LNQ_CASE(10)
+  PTB_LNQ_CASE(12)
+  PTB_LNQ_CASE(16)
+#undef PTB_LNQ_CASE
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_quantize_rows(const __nv_bfloat16* src0, int64_t ld0, int n0,

@@ -33,6 +33,10 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
+// VPT: 16-byte vectors of the row per thread (the row cache is sized to the
+// hidden size, so that more CTAs fit on an SM: at H = 12288, 6 instead of 16
+// vectors per thread).
+template <int VPT>
 __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
     const __nv_bfloat16* __restrict__ beta, int hidden, float eps,
@@ -42,10 +46,10 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(
   const int nvec = hidden / 8;
   const uint4* src = reinterpret_cast<const uint4*>(x + row * hidden);
 
-  uint4 cache[kLnMaxVec];
+  uint4 cache[VPT];
   float sum = 0.f;
 #pragma unroll
-  for (int j = 0; j < kLnMaxVec; ++j) {
+  for (int j = 0; j < VPT; ++j) {
     const int v = threadIdx.x + j * kLnThreads;
     if (v < nvec) {
       cache[j] = __ldcs(src + v);
@@ -58,7 +62,7 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(
 
   float sq = 0.f;
 #pragma unroll
-  for (int j = 0; j < kLnMaxVec; ++j) {
+  for (int j = 0; j < VPT; ++j) {
     const int v = threadIdx.x + j * kLnThreads;
     if (v < nvec) {
       const uint32_t w[4] = {cache[j].x, cache[j].y, cache[j].z, cache[j].w};
@@ -78,7 +82,7 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(
   const uint4* b4 = reinterpret_cast<const uint4*>(beta);
   uint4* dst = reinterpret_cast<uint4*>(out + row * hidden);
 #pragma unroll
-  for (int j = 0; j < kLnMaxVec; ++j) {
+  for (int j = 0; j < VPT; ++j) {
     const int v = threadIdx.x + j * kLnThreads;
     if (v < nvec) {
       const uint4 gv = __ldg(g4 + v);
@@ -106,9 +110,25 @@ cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* gamma,
   if (hidden % 8 != 0 || hidden / 8 > kLnMaxVec * kLnThreads) return cudaErrorInvalidValue;
   if (rows <= 0) return cudaSuccess;
   if (rows > 0x7fffffff) return cudaErrorInvalidValue;
-  layernorm_kernel<<<static_cast<unsigned>(rows), kLnThreads, 0, stream>>>(x, gamma, beta, hidden,
-                                                                           eps, out, stats);
-  return cudaGetLastError();
+  const int vpt = (hidden / 8 + kLnThreads - 1) / kLnThreads;
+  const unsigned grid = static_cast<unsigned>(rows);
+#define PTB_LN_CASE(V)                                                                         \
+  if (vpt <= V) {                                                                               \
+    layernorm_kernel<V><<<grid, kLnThreads, 0, stream>>>(x, gamma, beta, hidden, eps, out,     \
+                                                         stats);                               \
+    return cudaGetLastError();                                                                  \
+  }
+  PTB_LN_CASE(1)
+  PTB_LN_CASE(2)
+  PTB_LN_CASE(3)
+  PTB_LN_CASE(4)
+  PTB_LN_CASE(6)
+  PTB_LN_CASE(8)
+  PTB_LN_CASE(10)
+  PTB_LN_CASE(12)
+  PTB_LN_CASE(16)
+#undef PTB_LN_CASE
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace ptb
