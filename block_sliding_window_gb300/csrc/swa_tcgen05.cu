@@ -330,14 +330,19 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
           break;
         }
         tc_fence_after();
+        // Raw scores q.k: both halves of the row are loaded before one wait,
+        // and the scale goes into the exponent's FMA (the row max is taken on
+        // raw scores; the scale is positive).
+        static_assert(BKV == 64, "two 32-column TMEM loads per score row");
+        uint32_t raw0[32], raw1[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + C::s_col(x, buf), raw0);
+        tmem_ld_32x32b_x32(tmem + lane_base + C::s_col(x, buf) + 32, raw1);
+        tmem_ld_wait();
         float v[BKV];
 #pragma unroll
-        for (int c = 0; c < BKV; c += 32) {
-          uint32_t raw[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + C::s_col(x, buf) + c, raw);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[c + e] = __uint_as_float(raw[e]) * a.scale_log2;
+        for (int e = 0; e < 32; ++e) {
+          v[e] = __uint_as_float(raw0[e]);
+          v[32 + e] = __uint_as_float(raw1[e]);
         }
         const bool interior = (key0 + BKV - 1 <= i) && (key0 >= i - a.window + 1);
         if (!interior) {
@@ -354,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
         float mx = -INFINITY;
 #pragma unroll
         for (int e = 0; e < BKV; ++e) mx = fmaxf(mx, v[e]);
+        mx *= a.scale_log2;  // row max in the log2 domain
         // Raise the reference max only when the row max passes it by 2^8.
         float alpha = 1.f;
         const bool raise = mx > m_ref + kRescaleLog2;
@@ -367,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
         uint32_t pk[BKV / 2];
 #pragma unroll
         for (int e = 0; e < BKV; e += 2) {
-          const float p0 = fast_exp2(v[e] - m_use);
-          const float p1 = fast_exp2(v[e + 1] - m_use);
+          const float p0 = fast_exp2(fmaf(v[e], a.scale_log2, -m_use));
+          const float p1 = fast_exp2(fmaf(v[e + 1], a.scale_log2, -m_use));
           rs += p0 + p1;
           pk[e / 2] = pack_bf16x2(p0, p1);
         }
