@@ -8,7 +8,7 @@
 //   dgamma = sum over rows of dxn * xh,   dbeta = sum over rows of dxn.
 // Three launches, all deterministic:
 //   ln_bwd_rows_kernel     one CTA per row: dx (two block reductions).
-//   ln_bwd_columns_kernel  one thread per column and chunk of 128 rows:
+//   ln_bwd_columns_kernel  one thread per column and chunk of 32 rows:
 //                          partial sums of dxn * xh and dxn in row order.
 //   ln_bwd_reduce_kernel   one thread per column: the chunk partials in order.
 #include "ptb_device.cuh"
@@ -17,7 +17,7 @@ namespace ptb {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kChunkRows = 128;
+constexpr int kChunkRows = 32;  // rows per column partial (more CTAs in flight)
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
@@ -100,6 +100,7 @@ __global__ void ln_bwd_columns_kernel(const __nv_bfloat16* __restrict__ x,
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kChunkRows;
   const int64_t r1 = r0 + kChunkRows < rows ? r0 + kChunkRows : rows;
   float sgx = 0.f, sd = 0.f;
+#pragma unroll 8
   for (int64_t r = r0; r < r1; ++r) {
     const float2 st = __ldg(stats + r);
     const float d = __ldg(dxn + r * hidden + c);

@@ -490,28 +490,39 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
   }
 }
 
-// delta_i = sum_c dO_ic * o_ic for every (batch entry, head, row): one
-// thread per row, 16-byte loads.
+// delta_i = sum_c dO_ic * o_ic for every (batch entry, head, row): eight
+// lanes per row, lane j taking the 16-byte chunks j, j + 8, ... of the row
+// (head_dim / 8 chunks), summed by shuffles within the eight lanes.
 __global__ void swa_delta_kernel(const SwaBwdArgs a) {
   const int64_t rows = static_cast<int64_t>(a.batch) * a.heads * a.seq;
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < rows;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int i = static_cast<int>(idx % a.seq);
-    const int64_t bh = idx / a.seq;
-    const int h = static_cast<int>(bh % a.heads);
-    const int b = static_cast<int>(bh / a.heads);
-    const uint4* o = reinterpret_cast<const uint4*>(a.o + b * a.o_sb + h * a.o_sh + i * a.o_ss);
-    const uint4* g = reinterpret_cast<const uint4*>(a.dout + b * a.do_sb + h * a.do_sh +
-                                                    i * a.do_ss);
+  // Every lane of a warp runs the same number of iterations (the bound is a
+  // multiple of 4 and so is the stride), so the shuffles see all 32 lanes.
+  const int64_t bound = (rows + 3) & ~static_cast<int64_t>(3);
+  const int sub = threadIdx.x & 7;
+  const int chunks = a.head_dim / 8;
+  for (int64_t idx = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 3;
+       idx < bound; idx += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 3) {
     float acc = 0.f;
-    for (int v = 0; v < a.head_dim / 8; ++v) {
-      const uint4 x = __ldg(o + v), y = __ldg(g + v);
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+    if (idx < rows) {
+      const int i = static_cast<int>(idx % a.seq);
+      const int64_t bh = idx / a.seq;
+      const int h = static_cast<int>(bh % a.heads);
+      const int b = static_cast<int>(bh / a.heads);
+      const uint4* o = reinterpret_cast<const uint4*>(a.o + b * a.o_sb + h * a.o_sh + i * a.o_ss);
+      const uint4* g = reinterpret_cast<const uint4*>(a.dout + b * a.do_sb + h * a.do_sh +
+                                                      i * a.do_ss);
+      for (int c = sub; c < chunks; c += 8) {
+        const uint4 x = __ldg(o + c), y = __ldg(g + c);
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        acc += bf16_lo(xs[e]) * bf16_lo(ys[e]) + bf16_hi(xs[e]) * bf16_hi(ys[e]);
+        for (int e = 0; e < 4; ++e)
+          acc += bf16_lo(xs[e]) * bf16_lo(ys[e]) + bf16_hi(xs[e]) * bf16_hi(ys[e]);
+      }
     }
-    a.delta[idx] = acc;
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (idx < rows && sub == 0) a.delta[idx] = acc;
   }
 }
 
@@ -570,8 +581,8 @@ cudaError_t launch_swa_backward(const SwaBwdArgs& a, cudaStream_t stream) {
   if (a.seq <= 0 || a.batch <= 0 || a.heads <= 0) return cudaSuccess;
   const int64_t rows = static_cast<int64_t>(a.batch) * a.heads * a.seq;
   {
-    const int64_t blocks = (rows + 255) / 256;
-    const int grid = static_cast<int>(blocks < 8 * a.sms ? blocks : 8 * a.sms);
+    const int64_t blocks = (rows * 8 + 255) / 256;
+    const int grid = static_cast<int>(blocks < 16 * a.sms ? blocks : 16 * a.sms);
     swa_delta_kernel<<<grid, 256, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

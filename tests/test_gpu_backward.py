@@ -244,3 +244,22 @@ def test_ptb_backward_full_size_sampled(ptb_lib, name):
                    f_sel, r_sel)
     for k in want:
         assert_grad_close(got[k], want[k], f"{name} {k} (sampled)")
+
+
+def test_swa_long_sequence_forward_and_backward(ptb_lib):
+    """A long sequence (6144 positions, window 1500, d = 64): many query and
+    key blocks per item range, both kernels' band edges far from the
+    sequence ends.  Forward output, LSE and all three gradients against the
+    oracle."""
+    b, h, s, d, w = 1, 1, 6144, 64, 1500
+    q, k, v = workloads.swa_inputs(b, h, s, d, seed=61)
+    dout = workloads.normal_bf16((b, h, s, d), seed=62)
+    qc, kc, vc, dc = (t.cuda() for t in (q, k, v, dout))
+    o, lse = ptb_lib.swa_attention_lse(qc, kc, vc, w)
+    dq, dk, dv = ptb_lib.swa_attention_backward(qc, kc, vc, o, dc, lse, w)
+    torch.cuda.synchronize()
+    scale = 1.0 / math.sqrt(d)
+    assert_grad_close(o, oracle.swa(q, k, v, w, scale), "long SWA o")
+    want = oracle.swa_backward(q, k, v, dout, w, scale)
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), want):
+        assert_grad_close(got, ref, f"long SWA {name}")
