@@ -1,8 +1,11 @@
-// C ABI of libptb (declared in include/ptb.h): argument checks, tensor-map
-// encoding, the per-device workspace arena and status word, and the launch
-// sequence of the parallel transformer block forward pass
+// C ABI of libptb (declared in include/ptb.h), common part and forward pass:
+// argument checks, tensor-map encoding, the GEMM launch plumbing, the
+// per-device workspace arena and status word, and the launch sequence of the
+// parallel transformer block forward pass
 //   y = x + Attn(LN(x)) + MLP(LN(x))
-// (MegaScale study notes, ch.2 §2.2, PTB row).
+// (MegaScale study notes, ch.2 §2.2, PTB row).  The attention operator, the
+// FP8 variant and the training entry points are in api_swa.cu, api_fp8.cu
+// and api_train.cu.
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -10,34 +13,20 @@
 #include <cstring>
 #include <mutex>
 
+#include "api_internal.h"
 #include "ptb_device.cuh"
 
 namespace ptb {
-namespace {
+namespace api {
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kAlign = 256;
 
 __device__ unsigned g_status_word;
 
-struct DeviceState {
-  bool ready = false;
-  int sms = 0;
-  // 256 x 256 CTA-pair GEMM tiles: -1 automatic, 0 never, 1 wherever they
-  // apply (environment variable PTB_GEMM_PAIRS=0 / 1 overrides the default).
-  int pairs = -1;
-  unsigned* status = nullptr;
-  void* arena = nullptr;
-  size_t arena_bytes = 0;
-};
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Per-device set-up: SM count, device status word, architecture check and the
 // driver's tensor-map encoder.  Returns PTB_OK and fills *out.
@@ -169,28 +158,6 @@ void apply_plan(GemmArgs& a, int64_t num_kb, int sms, void* scratch, size_t scra
   }
 }
 
-const __nv_bfloat16* bf(const ptb_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
-__nv_bfloat16* bf(ptb_bf16* p) { return reinterpret_cast<__nv_bfloat16*>(p); }
-
-bool head_dim_ok(int64_t d) { return d == 16 || d == 32 || d == 64 || d == 96 || d == 128; }
-
-// One GEMM of the layer: C[M, N] = A[M, K] B[N, K]^T with
-//   A = [a0 | a1] split along K at k0 (k1 == 0: a0 only), and
-//   B = [b0 ; b1] split along N at n0 (n1 == 0: b0 only)
-// -- at most one split at a time.  In a K split b0 is [N, k0] and b1 is
-// [N, k1]; in an N split a0 is [M, K] and b0, b1 are [n0, K], [n1, K].
-struct GemmSpec {
-  const ptb_bf16 *a0, *a1, *b0, *b1;
-  int64_t lda0, lda1, k0, k1, n0, n1;
-  // e4m3 operands (a0, b0 then point at bytes): one scale per A row and per B row.
-  bool fp8 = false;
-  const float* a_scale = nullptr;
-  const float* b_scale = nullptr;
-  int64_t n() const { return n0 + n1; }
-  int64_t k() const { return k0 + k1; }
-  int64_t kb() const { return k() / (fp8 ? 128 : 64); }
-  int block_n() const { return n1 ? pick_block_n(n0, n1) : pick_block_n(n0, n0); }
-};
 
 GemmSpec spec_fp8(const void* a, int64_t lda, int64_t k, const void* b, int64_t n,
                   const float* a_scale, const float* b_scale) {
@@ -214,8 +181,8 @@ size_t spec_scratch(const GemmSpec& g, int64_t tokens, int sms) {
 
 ptb_status gemm_run(DeviceState* ds, const GemmSpec& g, int64_t tokens, ptb_bf16* out, int64_t ldo,
                     const ptb_bf16* resid, int64_t ldr, int64_t gelu_col, void* scratch,
-                    size_t scratch_bytes, cudaStream_t stream, ptb_bf16* aux = nullptr,
-                    int64_t ld_aux = 0, bool training = false) {
+                    size_t scratch_bytes, cudaStream_t stream, ptb_bf16* aux,
+                    int64_t ld_aux, bool training) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.block_n = g.block_n();
@@ -293,38 +260,11 @@ ptb_status gemm_out_down(DeviceState* ds, const ptb_bf16* ctx, int64_t ld_ctx, c
                          int64_t ld_g, const ptb_bf16* w_o, const ptb_bf16* w_down,
                          const ptb_bf16* x, int64_t tokens, int64_t hidden, int64_t ffn,
                          ptb_bf16* y, void* scratch, size_t scratch_bytes, cudaStream_t stream,
-                         bool training = false) {
+                         bool training) {
   return gemm_run(ds, spec_out_down(ctx, ld_ctx, g, ld_g, w_o, w_down, hidden, ffn), tokens, y,
                   hidden, x, hidden, hidden, scratch, scratch_bytes, stream, nullptr, 0, training);
 }
 
-// A GEMM of the backward pass, C[M, N] = A[M, K] B[N, K]^T, with operands
-// read in place from row-major matrices:
-//   A K-major:  a_i stored [M, K_i] (row stride lda_i);  A MN-major: [K_i, M].
-//   B K-major:  b_i stored [N_i, K] or [N, K_i];  B MN-major: [K, N_i] or [K_i, N].
-// A and B may be split in two along K at k_split (a0/b0 before, a1/b1
-// after), or B along N at n_split; at most one split (0 = none).
-struct GemmCall {
-  int layout = kLayoutKK;
-  int epilogue = kEpiF32;
-  int64_t M = 0, N = 0, K = 0;
-  const ptb_bf16 *a0 = nullptr, *a1 = nullptr, *b0 = nullptr, *b1 = nullptr;
-  int64_t lda0 = 0, lda1 = 0, ldb0 = 0, ldb1 = 0;
-  int64_t k_split = 0, n_split = 0;
-  void* out = nullptr;
-  int64_t ld_out = 0;
-  void* out1 = nullptr;
-  int64_t ld_out1 = 0;
-  int64_t out_split_col = 0, out_split_row = 0;  // 0 = no split
-  ptb_bf16* aux = nullptr;
-  int64_t ld_aux = 0;
-  int64_t gelu_col = 0;
-  bool a_keep = false, b_keep = false;
-  int block_n() const {
-    return n_split ? pick_block_n(n_split, N - n_split) : pick_block_n(N, N);
-  }
-  int64_t kb() const { return (K + 63) / 64; }
-};
 
 // 2-D bf16 tensor map with boxes of 64 x 64 over a row-major [outer, inner]
 // matrix (an MN-major operand: inner = M or N, outer = K).
@@ -474,11 +414,11 @@ __global__ void wait_probe_kernel(uint64_t limit_ns, unsigned* status) {
   }
 }
 
-}  // namespace
+}  // namespace api
 
 bool make_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                      const uint64_t* strides_bytes, const uint32_t* box) {
-  if (!g_encode || rank < 1 || rank > 5) return false;
+  if (!api::g_encode || rank < 1 || rank > 5) return false;
   cuuint64_t d[5], st[4];
   cuuint32_t b[5], e[5];
   for (int i = 0; i < rank; ++i) {
@@ -487,20 +427,21 @@ bool make_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_
     e[i] = 1;
     if (i + 1 < rank) st[i] = strides_bytes[i];
   }
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, b, e,
+  return api::g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, b, e,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t launch_wait_probe(uint64_t limit_ns, unsigned* status, cudaStream_t stream) {
-  wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
+  api::wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
   return cudaGetLastError();
 }
 
 }  // namespace ptb
 
 using namespace ptb;
+using namespace ptb::api;
 
 extern "C" {
 
@@ -536,7 +477,7 @@ size_t ptb_gemm_workspace_size(int64_t tokens, int64_t hidden, int64_t ffn) {
 }  // extern "C"
 
 namespace ptb {
-namespace {
+namespace api {
 
 // Argument checks shared by the layer entry points (before any device use).
 ptb_status check_layer(const void* const* ptrs, int nptrs, int64_t batch, int64_t seq,
@@ -605,146 +546,7 @@ SwaArgs swa_over_u(DeviceState* ds, ptb_bf16* u, int64_t ldu, int64_t batch, int
   return sa;
 }
 
-// Saved activations of ptb_forward_train, in this order, each region
-// starting on a kAlign boundary.
-struct SavedLayout {
-  size_t xn, stats, u, z, ctx, lse, total;
-};
-
-SavedLayout saved_layout(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int64_t heads) {
-  const size_t t = static_cast<size_t>(batch) * static_cast<size_t>(seq);
-  SavedLayout l;
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    const size_t at = off;
-    off += round_up(bytes, kAlign);
-    return at;
-  };
-  l.xn = take(t * hidden * 2);
-  l.stats = take(t * 8);
-  l.u = take(t * (3 * hidden + ffn) * 2);
-  l.z = take(t * ffn * 2);
-  l.ctx = take(t * hidden * 2);
-  l.lse = take(static_cast<size_t>(batch) * heads * seq * 4);
-  l.total = off;
-  return l;
-}
-
-// The four GEMMs of the backward pass (pointers left null: for sizing).
-GemmCall call_dgrad_out(int64_t t, int64_t h, int64_t f) {  // [dctx | dG] = dy [W_o | W_down]
-  GemmCall c;
-  c.layout = kLayoutKN;
-  c.epilogue = kEpiDgelu;
-  c.M = t, c.N = h + f, c.K = h, c.n_split = h;
-  c.lda0 = h, c.ldb0 = h, c.ldb1 = f;
-  c.out_split_col = h, c.gelu_col = h;
-  c.a_keep = true;
-  return c;
-}
-GemmCall call_wgrad_out(int64_t t, int64_t h, int64_t f, int64_t ldu) {  // dy^T [ctx | G]
-  GemmCall c;
-  c.layout = kLayoutNN;
-  c.epilogue = kEpiF32;
-  c.M = h, c.N = h + f, c.K = t, c.n_split = h;
-  c.lda0 = h, c.ldb0 = h, c.ldb1 = ldu;
-  c.out_split_col = h;
-  c.a_keep = true;
-  return c;
-}
-GemmCall call_dgrad_in(int64_t t, int64_t h, int64_t f, int64_t ldu) {  // dU1 [W_qkv ; W_up]
-  GemmCall c;
-  c.layout = kLayoutKN;
-  c.epilogue = kEpiF32;
-  c.M = t, c.N = h, c.K = ldu, c.k_split = 3 * h;
-  c.lda0 = ldu, c.lda1 = ldu, c.ldb0 = h, c.ldb1 = h;
-  (void)f;
-  return c;
-}
-GemmCall call_wgrad_in(int64_t t, int64_t h, int64_t f, int64_t ldu) {  // dU1^T xn
-  GemmCall c;
-  c.layout = kLayoutNN;
-  c.epilogue = kEpiF32;
-  c.M = ldu, c.N = h, c.K = t;
-  c.lda0 = ldu, c.ldb0 = h;
-  c.out_split_row = 3 * h;
-  c.b_keep = true;
-  (void)f;
-  return c;
-}
-
-struct BwdLayout {
-  size_t dctx, du1, delta, dxn, ln_part, gemm, total;
-};
-
-BwdLayout bwd_layout(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int64_t heads,
-                     int sms) {
-  const int64_t t = batch * seq, ldu = 3 * hidden + ffn;
-  BwdLayout l;
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    const size_t at = off;
-    off += round_up(bytes, kAlign);
-    return at;
-  };
-  l.dctx = take(static_cast<size_t>(t) * hidden * 2);
-  l.du1 = take(static_cast<size_t>(t) * ldu * 2);
-  l.delta = take(static_cast<size_t>(batch) * heads * seq * 4);
-  l.dxn = take(static_cast<size_t>(t) * hidden * 4);
-  l.ln_part = take(static_cast<size_t>(ln_backward_chunks(t)) * 2 * hidden * 4);
-  size_t g = 0;
-  for (const GemmCall& c : {call_dgrad_out(t, hidden, ffn), call_wgrad_out(t, hidden, ffn, ldu),
-                            call_dgrad_in(t, hidden, ffn, ldu), call_wgrad_in(t, hidden, ffn, ldu)}) {
-    const size_t b = call_scratch(c, sms);
-    g = b > g ? b : g;
-  }
-  l.gemm = take(g);
-  l.total = off;
-  return l;
-}
-
-ptb_status check_saved(const void* saved, size_t saved_bytes, const SavedLayout& l) {
-  if (!saved) return PTB_ERR_ARG;
-  if (!aligned(saved, kAlign)) return PTB_ERR_ALIGN;
-  if (saved_bytes < l.total) return PTB_ERR_WORKSPACE;
-  return PTB_OK;
-}
-
-SwaBwdArgs swa_bwd_args(DeviceState* ds, const ptb_bf16* u, const ptb_bf16* ctx,
-                        const ptb_bf16* dctx, ptb_bf16* du1, const float* lse, float* delta,
-                        int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
-                        int32_t window) {
-  const int64_t d = hidden / heads, ldu = 3 * hidden + ffn;
-  SwaBwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.q = bf(u);
-  a.k = bf(u) + hidden;
-  a.v = bf(u) + 2 * hidden;
-  a.o = bf(ctx);
-  a.dout = bf(dctx);
-  a.dq = bf(du1);
-  a.dk = bf(du1) + hidden;
-  a.dv = bf(du1) + 2 * hidden;
-  a.q_sb = a.k_sb = a.v_sb = a.dq_sb = a.dk_sb = a.dv_sb = seq * ldu;
-  a.q_sh = a.k_sh = a.v_sh = a.dq_sh = a.dk_sh = a.dv_sh = d;
-  a.q_ss = a.k_ss = a.v_ss = a.dq_ss = a.dk_ss = a.dv_ss = ldu;
-  a.o_sb = a.do_sb = seq * hidden;
-  a.o_sh = a.do_sh = d;
-  a.o_ss = a.do_ss = hidden;
-  a.lse = lse;
-  a.delta = delta;
-  a.batch = static_cast<int>(batch);
-  a.heads = heads;
-  a.seq = static_cast<int>(seq);
-  a.head_dim = static_cast<int>(d);
-  a.window = window;
-  a.scale = 1.0f / std::sqrt(static_cast<float>(d));
-  a.scale_log2 = a.scale * 1.4426950408889634f;
-  a.status = ds->status;
-  a.sms = ds->sms;
-  return a;
-}
-
-}  // namespace
+}  // namespace api
 }  // namespace ptb
 
 extern "C" {
@@ -928,71 +730,6 @@ ptb_status ptb_release_workspace(void) {
   return PTB_OK;
 }
 
-ptb_status swa_attention_strided(const ptb_bf16* q, int64_t q_sb, int64_t q_sh, int64_t q_ss,
-                                 const ptb_bf16* k, int64_t k_sb, int64_t k_sh, int64_t k_ss,
-                                 const ptb_bf16* v, int64_t v_sb, int64_t v_sh, int64_t v_ss,
-                                 ptb_bf16* o, int64_t o_sb, int64_t o_sh, int64_t o_ss,
-                                 int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
-                                 int32_t window, float scale, ptb_stream stream) {
-  if (batch > 65535 || seq > (1ll << 30)) return PTB_ERR_SHAPE;
-  SwaArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.q = bf(q);
-  a.k = bf(k);
-  a.v = bf(v);
-  a.o = bf(o);
-  a.q_sb = q_sb; a.q_sh = q_sh; a.q_ss = q_ss;
-  a.k_sb = k_sb; a.k_sh = k_sh; a.k_ss = k_ss;
-  a.v_sb = v_sb; a.v_sh = v_sh; a.v_ss = v_ss;
-  a.o_sb = o_sb; a.o_sh = o_sh; a.o_ss = o_ss;
-  a.batch = static_cast<int>(batch);
-  a.heads = heads;
-  a.seq = static_cast<int>(seq);
-  a.head_dim = head_dim;
-  a.window = window;
-  return swa_impl(a, scale, static_cast<cudaStream_t>(stream));
-}
-
-static ptb_status swa_contiguous(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v,
-                                 int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
-                                 int32_t window, float scale, ptb_bf16* o, int32_t* counts,
-                                 ptb_stream stream) {
-  if (batch > 65535 || seq > (1ll << 30) || head_dim < 1) return batch < 1 ? PTB_ERR_ARG
-                                                                           : PTB_ERR_SHAPE;
-  if (o == q || o == k || o == v) return PTB_ERR_ARG;
-  SwaArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.q = bf(q);
-  a.k = bf(k);
-  a.v = bf(v);
-  a.o = bf(o);
-  const int64_t ss = head_dim, sh = seq * head_dim, sb = heads * seq * head_dim;
-  a.q_sb = a.k_sb = a.v_sb = a.o_sb = sb;
-  a.q_sh = a.k_sh = a.v_sh = a.o_sh = sh;
-  a.q_ss = a.k_ss = a.v_ss = a.o_ss = ss;
-  a.batch = static_cast<int>(batch);
-  a.heads = heads;
-  a.seq = static_cast<int>(seq);
-  a.head_dim = head_dim;
-  a.window = window;
-  a.counts = counts;
-  return swa_impl(a, scale, static_cast<cudaStream_t>(stream));
-}
-
-ptb_status swa_attention(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v, int64_t batch,
-                         int32_t heads, int64_t seq, int32_t head_dim, int32_t window,
-                         float scale, ptb_bf16* o, ptb_stream stream) {
-  return swa_contiguous(q, k, v, batch, heads, seq, head_dim, window, scale, o, nullptr, stream);
-}
-
-ptb_status swa_attention_counts(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v,
-                                int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
-                                int32_t window, float scale, ptb_bf16* o, int32_t* counts,
-                                ptb_stream stream) {
-  if (!counts || !aligned(counts, 4)) return PTB_ERR_ARG;
-  return swa_contiguous(q, k, v, batch, heads, seq, head_dim, window, scale, o, counts, stream);
-}
-
 ptb_status ptb_layernorm(const ptb_bf16* x, const ptb_bf16* gamma, const ptb_bf16* beta,
                          int64_t rows, int64_t hidden, float eps, ptb_bf16* out,
                          ptb_stream stream) {
@@ -1056,356 +793,6 @@ ptb_status ptb_last_device_error(void) {
   if (cudaMemcpy(ds->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
     return PTB_ERR_LAUNCH;
   return static_cast<ptb_status>(word);
-}
-
-size_t ptb_forward_fp8_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn) {
-  if (batch < 1 || seq < 1 || hidden < 1 || ffn < 1) return 0;
-  const size_t t = static_cast<size_t>(batch) * static_cast<size_t>(seq);
-  size_t gemm = 0;
-  if (hidden % 64 == 0 && ffn % 64 == 0)
-    gemm = fp8_gemm_scratch(static_cast<int64_t>(t), hidden, ffn, current_sms());
-  return round_up(t * hidden, kAlign) + round_up(t * 4, kAlign) +
-         round_up(t * (3 * hidden + ffn) * 2, kAlign) + round_up(t * (hidden + ffn), kAlign) +
-         round_up(t * 4, kAlign) + gemm;
-}
-
-ptb_status ptb_prepare_fp8_weights(const ptb_bf16* w_qkv, const ptb_bf16* w_o,
-                                   const ptb_bf16* w_up, const ptb_bf16* w_down, int64_t hidden,
-                                   int64_t ffn, uint8_t* w1, float* s1, uint8_t* w2, float* s2,
-                                   ptb_stream stream_) {
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  const void* ptrs[] = {w_qkv, w_o, w_up, w_down, w1, s1, w2, s2};
-  for (const void* p : ptrs)
-    if (!p) return PTB_ERR_ARG;
-  for (const void* p : ptrs)
-    if (!aligned(p, 16)) return PTB_ERR_ALIGN;
-  if (hidden < 128 || ffn < 128) return PTB_ERR_ARG;
-  if (hidden % 128 || ffn % 128) return PTB_ERR_SHAPE;
-  DeviceState* ds = nullptr;
-  ptb_status st = device_state(&ds);
-  if (st != PTB_OK) return st;
-  const int h = static_cast<int>(hidden), f = static_cast<int>(ffn);
-  // w1 = [W_qkv ; W_up] row by row, w2 = [W_o | W_down] (rows concatenated along K).
-  if (launch_quantize_rows(bf(w_qkv), hidden, h, nullptr, 0, 0, 3 * hidden, 0, w1, s1, stream) !=
-          cudaSuccess ||
-      launch_quantize_rows(bf(w_up), hidden, h, nullptr, 0, 0, ffn, 3 * hidden, w1, s1, stream) !=
-          cudaSuccess ||
-      launch_quantize_rows(bf(w_o), hidden, h, bf(w_down), ffn, f, hidden, 0, w2, s2, stream) !=
-          cudaSuccess)
-    return PTB_ERR_LAUNCH;
-  return PTB_OK;
-}
-
-ptb_status ptb_forward_fp8_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
-                                  const ptb_bf16* ln_beta, const uint8_t* w1, const float* s1,
-                                  const uint8_t* w2, const float* s2, int64_t batch, int64_t seq,
-                                  int64_t hidden, int64_t ffn, int32_t heads, int32_t window,
-                                  ptb_bf16* y, void* workspace, size_t workspace_bytes,
-                                  ptb_stream stream_, void* const* events, int32_t n_events) {
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  const void* ptrs[] = {x, ln_gamma, ln_beta, w1, s1, w2, s2, y};
-  ptb_status st = check_layer(ptrs, 8, batch, seq, hidden, ffn, heads, window);
-  if (st != PTB_OK) return st;
-  // e4m3 k-blocks are 128 elements.
-  if (hidden % 128 || ffn % 128) return PTB_ERR_SHAPE;
-  if (events && n_events != 6) return PTB_ERR_ARG;
-  if (events)
-    for (int i = 0; i < 6; ++i)
-      if (!events[i]) return PTB_ERR_ARG;
-  auto mark = [&](int i) -> bool {
-    if (!events) return true;
-    if (cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) == cudaSuccess) return true;
-    cudaGetLastError();  // the failed record must not be reported by a later launch
-    return false;
-  };
-  DeviceState* ds = nullptr;
-  st = device_state(&ds);
-  if (st != PTB_OK) return st;
-  const int64_t tokens = batch * seq;
-  const size_t need = ptb_forward_fp8_workspace_size(batch, seq, hidden, ffn);
-  st = acquire_workspace(ds, need, workspace, workspace_bytes, &workspace);
-  if (st != PTB_OK) return st;
-  char* p = static_cast<char*>(workspace);
-  uint8_t* xn8 = reinterpret_cast<uint8_t*>(p);
-  p += round_up(tokens * hidden, kAlign);
-  float* sx = reinterpret_cast<float*>(p);
-  p += round_up(tokens * 4, kAlign);
-  ptb_bf16* u = reinterpret_cast<ptb_bf16*>(p);
-  p += round_up(tokens * (3 * hidden + ffn) * 2, kAlign);
-  uint8_t* a8 = reinterpret_cast<uint8_t*>(p);
-  p += round_up(tokens * (hidden + ffn), kAlign);
-  float* sa = reinterpret_cast<float*>(p);
-  p += round_up(tokens * 4, kAlign);
-  const size_t scratch_size = need - static_cast<size_t>(p - static_cast<char*>(workspace));
-  const int64_t ldu = 3 * hidden + ffn;
-
-  // 1. xn8, sx = quantize(LN(x)) per token
-  if (!mark(0)) return PTB_ERR_ARG;
-  if (launch_layernorm_fp8(bf(x), bf(ln_gamma), bf(ln_beta), tokens, static_cast<int>(hidden),
-                           1e-5f, xn8, sx, stream) != cudaSuccess)
-    return PTB_ERR_LAUNCH;
-  // 2. U = [xn W_qkv^T | gelu(xn W_up^T)] from e4m3 operands
-  if (!mark(1)) return PTB_ERR_ARG;
-  st = gemm_run(ds, spec_fp8(xn8, hidden, hidden, w1, ldu, sx, s1), tokens, u, ldu, nullptr, 0,
-                3 * hidden, p, scratch_size, stream);
-  if (st != PTB_OK) return st;
-  // 3. ctx = SWA(Q, K, V) over Q (bf16, as in ptb_forward)
-  if (!mark(2)) return PTB_ERR_ARG;
-  if (launch_swa(swa_over_u(ds, u, ldu, batch, seq, hidden, heads, window), stream) != cudaSuccess)
-    return PTB_ERR_LAUNCH;
-  // 4. a8, sa = quantize([ctx | G]) per token
-  if (!mark(3)) return PTB_ERR_ARG;
-  if (launch_quantize_rows(bf(u), ldu, static_cast<int>(hidden), bf(u) + 3 * hidden, ldu,
-                           static_cast<int>(ffn), tokens, 0, a8, sa, stream) != cudaSuccess)
-    return PTB_ERR_LAUNCH;
-  // 5. y = x + [ctx | G] [W_o | W_down]^T from e4m3 operands
-  if (!mark(4)) return PTB_ERR_ARG;
-  st = gemm_run(ds, spec_fp8(a8, hidden + ffn, hidden + ffn, w2, hidden, sa, s2), tokens, y,
-                hidden, x, hidden, hidden, p, scratch_size, stream);
-  if (st != PTB_OK) return st;
-  if (!mark(5)) return PTB_ERR_ARG;
-  return PTB_OK;
-}
-
-ptb_status ptb_forward_fp8(const ptb_bf16* x, const ptb_bf16* ln_gamma, const ptb_bf16* ln_beta,
-                           const uint8_t* w1, const float* s1, const uint8_t* w2, const float* s2,
-                           int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
-                           int32_t window, ptb_bf16* y, void* workspace, size_t workspace_bytes,
-                           ptb_stream stream) {
-  return ptb_forward_fp8_events(x, ln_gamma, ln_beta, w1, s1, w2, s2, batch, seq, hidden, ffn,
-                                heads, window, y, workspace, workspace_bytes, stream, nullptr, 0);
-}
-
-size_t ptb_train_saved_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,
-                            int32_t heads) {
-  if (batch < 1 || seq < 1 || hidden < 1 || ffn < 1 || heads < 1) return 0;
-  return saved_layout(batch, seq, hidden, ffn, heads).total;
-}
-
-ptb_status ptb_forward_train(const ptb_bf16* x, const ptb_bf16* ln_gamma, const ptb_bf16* ln_beta,
-                             const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
-                             const ptb_bf16* w_down, int64_t batch, int64_t seq, int64_t hidden,
-                             int64_t ffn, int32_t heads, int32_t window, ptb_bf16* y, void* saved,
-                             size_t saved_bytes, void* workspace, size_t workspace_bytes,
-                             ptb_stream stream_) {
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  const void* ptrs[] = {x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, y};
-  ptb_status st = check_layer(ptrs, 8, batch, seq, hidden, ffn, heads, window);
-  if (st != PTB_OK) return st;
-  const SavedLayout l = saved_layout(batch, seq, hidden, ffn, heads);
-  st = check_saved(saved, saved_bytes, l);
-  if (st != PTB_OK) return st;
-  DeviceState* ds = nullptr;
-  st = device_state(&ds);
-  if (st != PTB_OK) return st;
-  const int64_t tokens = batch * seq, ldu = 3 * hidden + ffn;
-  const size_t need = layer_gemm_scratch(tokens, hidden, ffn, ds->sms);
-  st = acquire_workspace(ds, need, workspace, workspace_bytes, &workspace);
-  if (st != PTB_OK) return st;
-  char* sv = static_cast<char*>(saved);
-  ptb_bf16* xn = reinterpret_cast<ptb_bf16*>(sv + l.xn);
-  float2* stats = reinterpret_cast<float2*>(sv + l.stats);
-  ptb_bf16* u = reinterpret_cast<ptb_bf16*>(sv + l.u);
-  ptb_bf16* z = reinterpret_cast<ptb_bf16*>(sv + l.z);
-  ptb_bf16* ctx = reinterpret_cast<ptb_bf16*>(sv + l.ctx);
-  float* lse = reinterpret_cast<float*>(sv + l.lse);
-  // 1. xn = LN(x), keeping (mean, rstd) per token
-  if (launch_layernorm(bf(x), bf(ln_gamma), bf(ln_beta), tokens, static_cast<int>(hidden), 1e-5f,
-                       bf(xn), stream, stats) != cudaSuccess)
-    return PTB_ERR_LAUNCH;
-  // 2. U = [xn W_qkv^T | gelu(Z)], Z = xn W_up^T kept
-  st = gemm_run(ds, spec_qkv_up(xn, w_qkv, w_up, hidden, ffn), tokens, u, ldu, nullptr, 0,
-                3 * hidden, workspace, need, stream, z, ffn, true);
-  if (st != PTB_OK) return st;
-  // 3. ctx = SWA(Q, K, V) into its own buffer (Q is needed again), with the
-  //    per-row log-sum-exp
-  SwaArgs sa = swa_over_u(ds, u, ldu, batch, seq, hidden, heads, window);
-  sa.o = bf(ctx);
-  sa.o_sb = seq * hidden;
-  sa.o_ss = hidden;
-  sa.lse = lse;
-  if (launch_swa(sa, stream) != cudaSuccess) return PTB_ERR_LAUNCH;
-  // 4. y = x + [ctx | G] [W_o | W_down]^T
-  return gemm_out_down(ds, ctx, hidden, u + 3 * hidden, ldu, w_o, w_down, x, tokens, hidden, ffn,
-                       y, workspace, need, stream, true);
-}
-
-size_t ptb_backward_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,
-                                   int32_t heads) {
-  if (batch < 1 || seq < 1 || hidden < 64 || ffn < 64 || heads < 1) return 0;
-  if (hidden % 64 || ffn % 64) return 0;
-  return bwd_layout(batch, seq, hidden, ffn, heads, current_sms()).total;
-}
-
-ptb_status ptb_backward_events(const ptb_bf16* dy, const ptb_bf16* x, const ptb_bf16* ln_gamma,
-                               const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
-                               const ptb_bf16* w_down, const void* saved, size_t saved_bytes,
-                               int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,
-                               int32_t heads, int32_t window, ptb_bf16* dx, float* dln_gamma,
-                               float* dln_beta, float* dw_qkv, float* dw_o, float* dw_up,
-                               float* dw_down, void* workspace, size_t workspace_bytes,
-                               ptb_stream stream_, void* const* events, int32_t n_events) {
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  const void* ptrs[] = {dy, x, ln_gamma, w_qkv, w_o, w_up, w_down, dx,
-                        dln_gamma, dln_beta, dw_qkv, dw_o, dw_up, dw_down};
-  ptb_status st = check_layer(ptrs, 14, batch, seq, hidden, ffn, heads, window);
-  if (st != PTB_OK) return st;
-  if (events && n_events != 7) return PTB_ERR_ARG;
-  if (events)
-    for (int i = 0; i < 7; ++i)
-      if (!events[i]) return PTB_ERR_ARG;
-  auto mark = [&](int i) -> bool {
-    if (!events) return true;
-    if (cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) == cudaSuccess) return true;
-    cudaGetLastError();  // the failed record must not be reported by a later launch
-    return false;
-  };
-  const SavedLayout l = saved_layout(batch, seq, hidden, ffn, heads);
-  st = check_saved(saved, saved_bytes, l);
-  if (st != PTB_OK) return st;
-  DeviceState* ds = nullptr;
-  st = device_state(&ds);
-  if (st != PTB_OK) return st;
-  const BwdLayout w = bwd_layout(batch, seq, hidden, ffn, heads, ds->sms);
-  st = acquire_workspace(ds, w.total, workspace, workspace_bytes, &workspace);
-  if (st != PTB_OK) return st;
-  const int64_t t = batch * seq, ldu = 3 * hidden + ffn;
-  const char* sv = static_cast<const char*>(saved);
-  const ptb_bf16* xn = reinterpret_cast<const ptb_bf16*>(sv + l.xn);
-  const float2* stats = reinterpret_cast<const float2*>(sv + l.stats);
-  const ptb_bf16* u = reinterpret_cast<const ptb_bf16*>(sv + l.u);
-  const ptb_bf16* z = reinterpret_cast<const ptb_bf16*>(sv + l.z);
-  const ptb_bf16* ctx = reinterpret_cast<const ptb_bf16*>(sv + l.ctx);
-  const float* lse = reinterpret_cast<const float*>(sv + l.lse);
-  char* ws = static_cast<char*>(workspace);
-  ptb_bf16* dctx = reinterpret_cast<ptb_bf16*>(ws + w.dctx);
-  ptb_bf16* du1 = reinterpret_cast<ptb_bf16*>(ws + w.du1);
-  float* delta = reinterpret_cast<float*>(ws + w.delta);
-  float* dxn = reinterpret_cast<float*>(ws + w.dxn);
-  float* ln_part = reinterpret_cast<float*>(ws + w.ln_part);
-  void* scratch = ws + w.gemm;
-  const size_t scratch_bytes = w.total - w.gemm;
-
-  // 1. [dctx | dZ] = dy [W_o | W_down], dZ = dG * gelu'(Z) written into dU1
-  if (!mark(0)) return PTB_ERR_ARG;
-  GemmCall c = call_dgrad_out(t, hidden, ffn);
-  c.a0 = dy, c.b0 = w_o, c.b1 = w_down;
-  c.out = dctx, c.ld_out = hidden, c.out1 = du1 + 3 * hidden, c.ld_out1 = ldu;
-  c.aux = const_cast<ptb_bf16*>(z), c.ld_aux = ffn;
-  st = gemm_call(ds, c, scratch, scratch_bytes, stream);
-  if (st != PTB_OK) return st;
-  // 2. [dW_o | dW_down] = dy^T [ctx | G]
-  if (!mark(1)) return PTB_ERR_ARG;
-  c = call_wgrad_out(t, hidden, ffn, ldu);
-  c.a0 = dy, c.b0 = ctx, c.b1 = u + 3 * hidden;
-  c.out = dw_o, c.ld_out = hidden, c.out1 = dw_down, c.ld_out1 = ffn;
-  st = gemm_call(ds, c, scratch, scratch_bytes, stream);
-  if (st != PTB_OK) return st;
-  // 3. [dQ | dK | dV] into dU1 from the banded attention backward
-  if (!mark(2)) return PTB_ERR_ARG;
-  if (launch_swa_backward(swa_bwd_args(ds, u, ctx, dctx, du1, lse, delta, batch, seq, hidden, ffn,
-                                       heads, window),
-                          stream) != cudaSuccess)
-    return PTB_ERR_LAUNCH;
-  // 4. dxn = dU1 [W_qkv ; W_up]   (fp32)
-  if (!mark(3)) return PTB_ERR_ARG;
-  c = call_dgrad_in(t, hidden, ffn, ldu);
-  c.a0 = du1, c.a1 = du1 + 3 * hidden, c.b0 = w_qkv, c.b1 = w_up;
-  c.out = dxn, c.ld_out = hidden;
-  st = gemm_call(ds, c, scratch, scratch_bytes, stream);
-  if (st != PTB_OK) return st;
-  // 5. [dW_qkv ; dW_up] = dU1^T xn
-  if (!mark(4)) return PTB_ERR_ARG;
-  c = call_wgrad_in(t, hidden, ffn, ldu);
-  c.a0 = du1, c.b0 = xn;
-  c.out = dw_qkv, c.ld_out = hidden, c.out1 = dw_up, c.ld_out1 = hidden;
-  st = gemm_call(ds, c, scratch, scratch_bytes, stream);
-  if (st != PTB_OK) return st;
-  // 6. dx = dy + LN backward of dxn; dgamma, dbeta
-  if (!mark(5)) return PTB_ERR_ARG;
-  st = launch_status(launch_layernorm_backward(bf(x), bf(ln_gamma), stats, dxn, bf(dy), t,
-                                               static_cast<int>(hidden), bf(dx), dln_gamma,
-                                               dln_beta, ln_part, stream));
-  if (st != PTB_OK) return st;
-  if (!mark(6)) return PTB_ERR_ARG;
-  return PTB_OK;
-}
-
-ptb_status ptb_backward(const ptb_bf16* dy, const ptb_bf16* x, const ptb_bf16* ln_gamma,
-                        const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
-                        const ptb_bf16* w_down, const void* saved, size_t saved_bytes,
-                        int64_t batch, int64_t seq, int64_t hidden, int64_t ffn, int32_t heads,
-                        int32_t window, ptb_bf16* dx, float* dln_gamma, float* dln_beta,
-                        float* dw_qkv, float* dw_o, float* dw_up, float* dw_down, void* workspace,
-                        size_t workspace_bytes, ptb_stream stream) {
-  return ptb_backward_events(dy, x, ln_gamma, w_qkv, w_o, w_up, w_down, saved, saved_bytes, batch,
-                             seq, hidden, ffn, heads, window, dx, dln_gamma, dln_beta, dw_qkv,
-                             dw_o, dw_up, dw_down, workspace, workspace_bytes, stream, nullptr, 0);
-}
-
-ptb_status swa_attention_lse(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v,
-                             int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
-                             int32_t window, float scale, ptb_bf16* o, float* lse,
-                             ptb_stream stream) {
-  if (!lse || !aligned(lse, 4)) return PTB_ERR_ARG;
-  if (batch < 1 || seq < 1 || heads < 1) return PTB_ERR_ARG;
-  if (batch > 65535 || seq > (1ll << 30)) return PTB_ERR_SHAPE;
-  if (o == q || o == k || o == v) return PTB_ERR_ARG;
-  SwaArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.q = bf(q), a.k = bf(k), a.v = bf(v), a.o = bf(o);
-  const int64_t ss = head_dim, sh = seq * head_dim, sb = heads * seq * head_dim;
-  a.q_sb = a.k_sb = a.v_sb = a.o_sb = sb;
-  a.q_sh = a.k_sh = a.v_sh = a.o_sh = sh;
-  a.q_ss = a.k_ss = a.v_ss = a.o_ss = ss;
-  a.batch = static_cast<int>(batch);
-  a.heads = heads;
-  a.seq = static_cast<int>(seq);
-  a.head_dim = head_dim;
-  a.window = window;
-  a.lse = lse;
-  return swa_impl(a, scale, static_cast<cudaStream_t>(stream));
-}
-
-ptb_status swa_attention_backward(const ptb_bf16* q, const ptb_bf16* k, const ptb_bf16* v,
-                                  const ptb_bf16* o, const ptb_bf16* dout, const float* lse,
-                                  int64_t batch, int32_t heads, int64_t seq, int32_t head_dim,
-                                  int32_t window, float scale, ptb_bf16* dq, ptb_bf16* dk,
-                                  ptb_bf16* dv, float* delta, ptb_stream stream) {
-  const void* ptrs[] = {q, k, v, o, dout, dq, dk, dv};
-  for (const void* p : ptrs)
-    if (!p) return PTB_ERR_ARG;
-  if (!lse || !delta || batch < 1 || seq < 1 || heads < 1 || window < 1) return PTB_ERR_ARG;
-  if (!head_dim_ok(head_dim)) return PTB_ERR_SHAPE;
-  if (batch > 65535 || seq > (1ll << 30) || batch * static_cast<int64_t>(heads) > 65535)
-    return PTB_ERR_SHAPE;
-  for (const void* p : ptrs)
-    if (!aligned(p, 16)) return PTB_ERR_ALIGN;
-  if (!aligned(lse, 4) || !aligned(delta, 4)) return PTB_ERR_ALIGN;
-  if (scale < 0.f || !std::isfinite(scale)) return PTB_ERR_ARG;
-  DeviceState* ds = nullptr;
-  ptb_status st = device_state(&ds);
-  if (st != PTB_OK) return st;
-  SwaBwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.q = bf(q), a.k = bf(k), a.v = bf(v), a.o = bf(o), a.dout = bf(dout);
-  a.dq = bf(dq), a.dk = bf(dk), a.dv = bf(dv);
-  const int64_t ss = head_dim, sh = seq * head_dim, sb = heads * seq * head_dim;
-  a.q_sb = a.k_sb = a.v_sb = a.o_sb = a.do_sb = a.dq_sb = a.dk_sb = a.dv_sb = sb;
-  a.q_sh = a.k_sh = a.v_sh = a.o_sh = a.do_sh = a.dq_sh = a.dk_sh = a.dv_sh = sh;
-  a.q_ss = a.k_ss = a.v_ss = a.o_ss = a.do_ss = a.dq_ss = a.dk_ss = a.dv_ss = ss;
-  a.lse = lse;
-  a.delta = delta;
-  a.batch = static_cast<int>(batch);
-  a.heads = heads;
-  a.seq = static_cast<int>(seq);
-  a.head_dim = head_dim;
-  a.window = window;
-  a.scale = scale == 0.f ? 1.0f / std::sqrt(static_cast<float>(head_dim)) : scale;
-  a.scale_log2 = a.scale * 1.4426950408889634f;
-  a.status = ds->status;
-  a.sms = ds->sms;
-  return launch_status(launch_swa_backward(a, static_cast<cudaStream_t>(stream)));
 }
 
 ptb_status ptb_set_gemm_pairs(int32_t mode, int32_t* previous) {
