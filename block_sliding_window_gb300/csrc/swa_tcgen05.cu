@@ -8,30 +8,37 @@
 //
 // Persistent kernel: one CTA per SM walks work items = (256-query block,
 // head, batch entry).  An item is two 128-row query tiles X = 0, 1 that share
-// every K/V tile.  320 threads:
+// every K/V tile.  352 threads:
 //   warp 0      TMA: the two Q tiles of an item, then the 64-key K and V
 //               tiles intersecting the item's band [q0 - w + 1, q0 + 255]
-//               (diagonal tile first) into a ring of 4 stages (d > 64; 6 for
+//               (diagonal tile first) into a ring of 5 stages (d > 64; 6 for
 //               d <= 64) that runs on across items.  d < 128 is read as
-//               64-wide boxes; columns
-//               past d are zero-filled by TMA.  (An L2 prefetch of the tiles
-//               four positions ahead was measured slightly slower.)
-//   warp 1      owns TMEM (512 columns: per query tile two 64-column score
-//               buffers and a d-column output accumulator); one thread issues
+//               64-wide boxes; columns past d are zero-filled by TMA.  (An L2
+//               prefetch of the tiles four positions ahead was measured
+//               slightly slower.)
+//   warps 1, 2  one MMA-issuing thread per query tile X (warp 1 also owns
+//               TMEM: 512 columns, per query tile two 64-column score
+//               buffers and a d-column output accumulator).  Thread X issues
 //                 S_X = Q_X K_j^T   (M 128, N 64, K d)
-//                 O_X += P_X V_j    (M 128, N d, K 64; V read in place as an
-//                                    MN-major operand)
-//               skipping any (tile, X) pair that lies wholly outside the band.
-//   warps 2..9  two softmax warpgroups, one per query tile, one query row per
+//                 O_X += P_X V_j    (M 128, N d, K 64; P read from TMEM, V
+//                                    read in place as an MN-major operand)
+//               skipping any tile that lies wholly outside its band.  Score
+//               tile n + 2 reuses the buffer of tile n, so it is issued only
+//               once P V n has finished.  A single thread issues at most one
+//               tcgen05.mma every ~75 cycles, whatever its N (measured), so
+//               one thread per query tile doubles the rate at which these
+//               small MMAs reach the tensor pipe.
+//   warps 3..10 two softmax warpgroups, one per query tile, one query row per
 //               thread (TMEM lane = row).  Per tile: read the score row, mask
 //               only on band-edge tiles, exponentiate in the log2 domain
 //               against a reference max that is raised only when the row max
 //               exceeds it by more than 8 (so P <= 2^8 in bf16); raising it
 //               rescales the running sum and the output row in TMEM.  The
-//               bf16 P row goes to shared memory (one buffer per query tile)
-//               in the 128-byte-swizzled operand layout; a softmax warp waits
-//               for a P V only to reuse the buffer (the previous tile's P V)
-//               or to rescale O.  At the end of an item O / l -> bf16.
+//               bf16 P row is written back into TMEM over the scores it came
+//               from (row = lane, two keys per column), where the P V MMA
+//               reads it as its A operand: P never passes through shared
+//               memory, and a softmax warp waits for a P V only to rescale O.
+//               At the end of an item O / l -> bf16.
 // Every mbarrier wait is bounded (see mbar_wait); on a timeout all roles
 // unwind, wait for their own copies and MMAs, free TMEM and return.
 #include "ptb_device.cuh"
@@ -42,7 +49,7 @@ namespace {
 constexpr int BQ = 128;       // rows per query tile (= MMA M)
 constexpr int QT = 2;         // query tiles per work item
 constexpr int BKV = 64;       // keys per K/V tile (= MMA N of S, K of PV)
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr float kRescaleLog2 = 8.0f;  // raise the reference max only past 2^8
 
 template <int D>
@@ -50,11 +57,8 @@ struct SwaCfg {
   static constexpr int kAtoms = (D + 63) / 64;          // 64-wide column blocks of d
   static constexpr int kQTileBytes = kAtoms * BQ * 128;
   static constexpr int kKVBytes = kAtoms * BKV * 128;   // one of K or V, one stage
-  static constexpr int kPBytes = BQ * BKV * 2;          // P of one query tile
-  // One P buffer per query tile (a P V is short, so the next tile's P rarely
-  // waits for it) leaves room for a deeper K/V ring.
-  static constexpr int kPBufs = 1;
-  static constexpr int kFixed = QT * kQTileBytes + QT * kPBufs * kPBytes + 512 + 1024;
+  // P never touches shared memory: it overwrites its own score buffer in TMEM.
+  static constexpr int kFixed = QT * kQTileBytes + 512 + 1024;
   static constexpr int kNSFit = (227 * 1024 - kFixed) / (2 * kKVBytes);
   static constexpr int kNS = kNSFit < 6 ? kNSFit : 6;  // K/V stages
   static constexpr int kSmemBytes = kFixed + kNS * 2 * kKVBytes;
@@ -112,7 +116,6 @@ template <int D, bool COUNTS>
 __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_constant__ SwaParams P) {
   using C = SwaCfg<D>;
   constexpr int NS = C::kNS;
-  constexpr int PB = C::kPBufs;
   const SwaArgs& a = P.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -120,17 +123,16 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
   uint8_t* sQ = smem;                               // [QT][kQTileBytes]
   uint8_t* sK = sQ + QT * C::kQTileBytes;           // [NS][kKVBytes]
   uint8_t* sV = sK + NS * C::kKVBytes;              // [NS][kKVBytes]
-  uint8_t* sP = sV + NS * C::kKVBytes;              // [QT][PB][kPBytes]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + QT * PB * C::kPBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NS * C::kKVBytes);
   uint64_t* q_full = bars;
   uint64_t* q_empty = q_full + 1;
   uint64_t* kv_full = q_empty + 1;      // [NS]
   uint64_t* kv_empty = kv_full + NS;    // [NS]
   uint64_t* s_full = kv_empty + NS;     // [QT][2]
-  uint64_t* p_full = s_full + 2 * QT;   // [QT][PB]
-  uint64_t* pv_done = p_full + PB * QT; // [QT][PB]
-  uint64_t* done_bar = pv_done + PB * QT;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* p_full = s_full + 2 * QT;   // [QT][2]: P in score buffer 0 / 1
+  uint64_t* pv_done = p_full + 2 * QT;  // [QT][2]: P V of score buffer 0 / 1
+  uint64_t* done_bar = pv_done + 2 * QT;  // [QT]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + QT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -138,20 +140,21 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    mbar_init(q_empty, QT);  // both MMA threads release Q
     for (int s = 0; s < NS; ++s) {
       mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&kv_empty[s], QT);  // and every K/V stage
     }
     for (int x = 0; x < QT; ++x) {
       mbar_init(&s_full[2 * x], 1);
       mbar_init(&s_full[2 * x + 1], 1);
-      for (int k = 0; k < PB; ++k) {
-        mbar_init(&p_full[PB * x + k], 4);
-        mbar_init(&pv_done[PB * x + k], 1);
-      }
+      mbar_init(&p_full[2 * x], 4);
+      mbar_init(&p_full[2 * x + 1], 4);
+      mbar_init(&pv_done[2 * x], 1);
+      mbar_init(&pv_done[2 * x + 1], 1);
     }
-    mbar_init(done_bar, 1);
+    mbar_init(&done_bar[0], 1);
+    mbar_init(&done_bar[1], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -216,22 +219,27 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
           mbar_wait(&kv_full[s], (armed_parity >> s) & 1u, &no_abort, a.status);
       if (q_count > 0) mbar_wait(q_full, (q_count - 1) & 1, &no_abort, a.status);
     }
-  } else if (warp == 1) {
+  } else if (warp <= QT) {
     // ------------------------------------------------------------- MMA --
+    // One issuing thread per query tile: a single thread issues at most one
+    // tcgen05.mma every ~75 cycles whatever its N, which is slower than the
+    // tensor pipe runs these small (N = 64, K = 16) MMAs; two threads feed
+    // it twice as fast.  Each thread observes every K/V stage in order and
+    // releases every stage and every Q tile (those barriers count both).
+    const int x = warp - 1;
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16(BQ, BKV);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(BQ, D) | (1u << 16);  // B (V) MN-major
       bool ok = true;
-      uint32_t kv_count = 0, q_count = 0;
-      uint32_t s_issued[QT] = {0, 0}, pv_issued[QT] = {0, 0};
-      const uint32_t q_addr = smem_addr(sQ);
+      uint32_t kv_count = 0, q_count = 0, s_issued = 0, pv_issued = 0;
+      const uint32_t qx = smem_addr(sQ + x * C::kQTileBytes);
       for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
         const Item it = decode_item(P, item);
         if (!mbar_wait(q_full, q_count & 1, abort_flag, a.status)) break;
         ++q_count;
         tc_fence_after();
-        bool first_pv[QT] = {true, true};
-        for (int j = 0; ok && j <= it.n_tiles; ++j) {
+        bool first_pv = true;
+        for (int j = 0; j <= it.n_tiles; ++j) {
           if (j < it.n_tiles) {
             const uint32_t kc = kv_count + j;
             const int st = kc % NS;
@@ -240,63 +248,63 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
               break;
             }
             tc_fence_after();
-            const int key0 = (it.kt_hi - j) * BKV;
-            const uint32_t k_addr = smem_addr(sK + st * C::kKVBytes);
-            for (int x = 0; x < QT; ++x) {
-              if (!tile_relevant(P, it, x, key0)) continue;
-              const int buf = s_issued[x] & 1;
-              const uint32_t d_tmem = tmem + C::s_col(x, buf);
-              const uint32_t qx = q_addr + x * C::kQTileBytes;
+            if (tile_relevant(P, it, x, (it.kt_hi - j) * BKV)) {
+              // Score buffer n % 2 still holds P number n - 2 until its P V ends.
+              const uint32_t n = s_issued;
+              if (n >= 2) {
+                if (!mbar_wait(&pv_done[2 * x + (n & 1)], ((n - 2) >> 1) & 1, abort_flag,
+                               a.status)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+              }
+              const uint32_t d_tmem = tmem + C::s_col(x, n & 1);
+              const uint32_t k_addr = smem_addr(sK + st * C::kKVBytes);
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t at = kk / 4, off = (kk % 4) * 32;
                 umma_bf16_ss(d_tmem, sw128_kmajor_desc(qx + at * BQ * 128 + off),
                              sw128_kmajor_desc(k_addr + at * BKV * 128 + off), idesc_s, kk > 0);
               }
-              umma_commit(&s_full[2 * x + buf]);
-              ++s_issued[x];
+              umma_commit(&s_full[2 * x + (n & 1)]);
+              ++s_issued;
+            } else {
+              umma_commit(&kv_empty[st]);  // this query tile never reads the stage
             }
-            if (j == it.n_tiles - 1) umma_commit(q_empty);  // Q is free once these finish
+            if (j == it.n_tiles - 1) umma_commit(q_empty);  // Q_X is free once these finish
           }
-          if (j >= 1) {
-            const int t = j - 1;
-            const uint32_t kc = kv_count + t;
-            const int st = kc % NS;
-            const int key0 = (it.kt_hi - t) * BKV;
-            const uint32_t v_addr = smem_addr(sV + st * C::kKVBytes);
-            for (int x = 0; x < QT; ++x) {
-              if (!tile_relevant(P, it, x, key0)) continue;
-              const uint32_t n = pv_issued[x];  // P V number n uses P buffer n % PB
-              const uint32_t pb = PB * x + n % PB, pph = (n / PB) & 1;
-              if (!mbar_wait(&p_full[pb], pph, abort_flag, a.status)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint32_t p_addr = smem_addr(sP + pb * C::kPBytes);
-              const uint32_t d_tmem = tmem + C::o_col(x);
-#pragma unroll
-              for (int kk = 0; kk < BKV / 16; ++kk)
-                umma_bf16_ss(d_tmem, sw128_kmajor_desc(p_addr + kk * 32),
-                             sw128_mnmajor_desc(v_addr + kk * 16 * 128, BKV * 128), idesc_pv,
-                             (!first_pv[x] || kk > 0) ? 1u : 0u);
-              umma_commit(&pv_done[pb]);
-              ++pv_issued[x];
-              first_pv[x] = false;
+          if (j >= 1 && tile_relevant(P, it, x, (it.kt_hi - (j - 1)) * BKV)) {
+            const int st = (kv_count + j - 1) % NS;
+            const uint32_t n = pv_issued;  // P number n sits in score buffer n % 2
+            if (!mbar_wait(&p_full[2 * x + (n & 1)], (n >> 1) & 1, abort_flag, a.status)) {
+              ok = false;
+              break;
             }
-            if (!ok) break;
+            tc_fence_after();
+            const uint32_t p_tmem = tmem + C::s_col(x, n & 1);
+            const uint32_t d_tmem = tmem + C::o_col(x);
+            const uint32_t v_addr = smem_addr(sV + st * C::kKVBytes);
+#pragma unroll
+            for (int kk = 0; kk < BKV / 16; ++kk)  // 16 keys = 8 packed P columns
+              umma_bf16_ts(d_tmem, p_tmem + kk * 8,
+                           sw128_mnmajor_desc(v_addr + kk * 16 * 128, BKV * 128), idesc_pv,
+                           (!first_pv || kk > 0) ? 1u : 0u);
+            umma_commit(&pv_done[2 * x + (n & 1)]);
             umma_commit(&kv_empty[st]);
+            ++pv_issued;
+            first_pv = false;
           }
         }
         kv_count += it.n_tiles;
       }
-      umma_commit(done_bar);
+      umma_commit(&done_bar[x]);
       volatile int no_abort = 0;
-      mbar_wait(done_bar, 0, &no_abort, a.status);
+      mbar_wait(&done_bar[x], 0, &no_abort, a.status);
     }
   } else {
     // --------------------------------------------------------- softmax --
-    const int x = (warp - 2) >> 2;      // query tile of this warpgroup
+    const int x = (warp - 1 - QT) >> 2;  // query tile of this warpgroup
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row in the query tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
@@ -304,11 +312,16 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
     uint32_t seen = 0;  // relevant tiles of this query tile so far (all items)
     bool ok = true;
 
-    // P V number n of this query tile is signalled on pv_done[x][n % PB];
-    // waits never lag a barrier by two phases (P V n + PB needs P n + PB,
-    // which is only written after this wait).
+    // P V number n of this query tile completes phase n / 2 of
+    // pv_done[x][n % 2].  A parity wait is exact only while its barrier is
+    // at most one phase behind or ahead of the awaited one: here P V n - 2
+    // has always finished (score tile n, already read, was issued after it)
+    // and P V n + 2 cannot start (it needs P n + 2 from this warpgroup).
+    // One barrier for both buffers would break this: waiting for the
+    // item's last P V while the one before it was still running would
+    // return at once.
     auto wait_pv = [&](uint32_t n) -> bool {
-      if (!mbar_wait_warp(&pv_done[PB * x + n % PB], (n / PB) & 1, abort_flag, a.status))
+      if (!mbar_wait_warp(&pv_done[2 * x + (n & 1)], (n >> 1) & 1, abort_flag, a.status))
         return false;
       tc_fence_after();
       return true;
@@ -379,21 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
           pk[e / 2] = pack_bf16x2(p0, p1);
         }
         l_run += rs;
-        // The P buffer was last read by P V number seen - PB.
-        if (seen >= static_cast<uint32_t>(PB) && !wait_pv(seen - PB)) {
-          ok = false;
-          break;
-        }
-        uint8_t* prow = sP + (PB * x + seen % PB) * C::kPBytes + r * 128;
-        // Row r of P: 64 keys = one 128-byte swizzled row; 16-byte chunk c
-        // sits at chunk position c ^ (r % 8).
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        // P (bf16 pairs) over the first 32 columns of the scores just read.
+        tmem_st_32x32b_x32(tmem + lane_base + C::s_col(x, buf), pk);
         if (any_pv && __any_sync(0xffffffffu, raise)) {
           // O must hold every earlier P V of this item before it is rescaled.
           if (!wait_pv(seen - 1)) {
+            tmem_st_wait();
             ok = false;
             break;
           }
@@ -415,12 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
             for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
             tmem_st_32x32b_x16(o_tmem, o);
           }
-          tmem_st_wait();
         }
-        fence_proxy_async_smem();
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[PB * x + seen % PB]);
+        if (lane == 0) mbar_arrive(&p_full[2 * x + buf]);
         any_pv = true;
         ++seen;
       }
