@@ -8,7 +8,7 @@
 //
 // Persistent kernel: one CTA per SM walks work items = (256-query block,
 // head, batch entry).  An item is two 128-row query tiles X = 0, 1 that share
-// every K/V tile.  352 threads:
+// every K/V tile.  416 threads:
 //   warp 0      TMA: the two Q tiles of an item, then the 64-key K and V
 //               tiles intersecting the item's band [q0 - w + 1, q0 + 255]
 //               (diagonal tile first) into a ring of 5 stages (d > 64; 6 for
@@ -16,19 +16,21 @@
 //               64-wide boxes; columns past d are zero-filled by TMA.  (An L2
 //               prefetch of the tiles four positions ahead was measured
 //               slightly slower.)
-//   warps 1, 2  one MMA-issuing thread per query tile X (warp 1 also owns
-//               TMEM: 512 columns, per query tile two 64-column score
-//               buffers and a d-column output accumulator).  Thread X issues
-//                 S_X = Q_X K_j^T   (M 128, N 64, K d)
-//                 O_X += P_X V_j    (M 128, N d, K 64; P read from TMEM, V
-//                                    read in place as an MN-major operand)
-//               skipping any tile that lies wholly outside its band.  Score
-//               tile n + 2 reuses the buffer of tile n, so it is issued only
-//               once P V n has finished.  A single thread issues at most one
-//               tcgen05.mma every ~75 cycles, whatever its N (measured), so
-//               one thread per query tile doubles the rate at which these
-//               small MMAs reach the tensor pipe.
-//   warps 3..10 two softmax warpgroups, one per query tile, one query row per
+//   warps 1..4  four MMA-issuing threads, two per query tile X (warp 1 also
+//               owns TMEM: 512 columns, per query tile two 64-column score
+//               buffers and a d-column output accumulator):
+//                 warps 1, 2   S_X = Q_X K_j^T   (M 128, N 64, K d)
+//                 warps 3, 4   O_X += P_X V_j    (M 128, N d, K 64; P read
+//                                               from TMEM, V read in place
+//                                               as an MN-major operand)
+//               skipping any tile that lies wholly outside the band of X.
+//               Score tile n + 2 reuses the buffer of tile n, so it is issued
+//               only once P V n has finished.  A single thread issues at most
+//               one tcgen05 instruction (MMA or commit) every ~75 cycles,
+//               whatever the MMA's N (measured), which is slower than the
+//               tensor pipe runs these small MMAs; four instruction streams
+//               keep it fed.
+//   warps 5..12 two softmax warpgroups, one per query tile, one query row per
 //               thread (TMEM lane = row).  Per tile: read the score row, mask
 //               only on band-edge tiles, exponentiate in the log2 domain
 //               against a reference max that is raised only when the row max
@@ -49,7 +51,7 @@ namespace {
 constexpr int BQ = 128;       // rows per query tile (= MMA M)
 constexpr int QT = 2;         // query tiles per work item
 constexpr int BKV = 64;       // keys per K/V tile (= MMA N of S, K of PV)
-constexpr int kThreads = 352;
+constexpr int kThreads = 416;
 constexpr float kRescaleLog2 = 8.0f;  // raise the reference max only past 2^8
 
 template <int D>
@@ -131,8 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
   uint64_t* s_full = kv_empty + NS;     // [QT][2]
   uint64_t* p_full = s_full + 2 * QT;   // [QT][2]: P in score buffer 0 / 1
   uint64_t* pv_done = p_full + 2 * QT;  // [QT][2]: P V of score buffer 0 / 1
-  uint64_t* done_bar = pv_done + 2 * QT;  // [QT]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + QT);
+  uint64_t* done_bar = pv_done + 2 * QT;  // [2 * QT]: one per issuing thread
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 2 * QT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -140,10 +142,10 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(q_empty, QT);  // both MMA threads release Q
+    mbar_init(q_empty, QT);  // both score threads release Q
     for (int s = 0; s < NS; ++s) {
       mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], QT);  // and every K/V stage
+      mbar_init(&kv_empty[s], QT);  // each query tile releases every K/V stage
     }
     for (int x = 0; x < QT; ++x) {
       mbar_init(&s_full[2 * x], 1);
@@ -153,8 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
       mbar_init(&pv_done[2 * x], 1);
       mbar_init(&pv_done[2 * x + 1], 1);
     }
-    mbar_init(&done_bar[0], 1);
-    mbar_init(&done_bar[1], 1);
+    for (int t = 0; t < 2 * QT; ++t) mbar_init(&done_bar[t], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -219,38 +220,51 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
           mbar_wait(&kv_full[s], (armed_parity >> s) & 1u, &no_abort, a.status);
       if (q_count > 0) mbar_wait(q_full, (q_count - 1) & 1, &no_abort, a.status);
     }
-  } else if (warp <= QT) {
+  } else if (warp <= 2 * QT) {
     // ------------------------------------------------------------- MMA --
-    // One issuing thread per query tile: a single thread issues at most one
-    // tcgen05.mma every ~75 cycles whatever its N, which is slower than the
-    // tensor pipe runs these small (N = 64, K = 16) MMAs; two threads feed
-    // it twice as fast.  Each thread observes every K/V stage in order and
-    // releases every stage and every Q tile (those barriers count both).
-    const int x = warp - 1;
+    // Four issuing threads: for each query tile X one issues its scores
+    // (warps 1, 2) and one its P V products (warps 3, 4).  A single thread
+    // issues at most one tcgen05 instruction (MMA or commit) every ~75
+    // cycles whatever the MMA's N, slower than the tensor pipe runs these
+    // small MMAs; split four ways the instruction streams keep it fed, and
+    // each query tile's chain S -> softmax -> P V -> S overlaps across them.
+    const bool pv_role = warp > QT;
+    const int x = pv_role ? warp - 1 - QT : warp - 1;
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16(BQ, BKV);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(BQ, D) | (1u << 16);  // B (V) MN-major
       bool ok = true;
-      uint32_t kv_count = 0, q_count = 0, s_issued = 0, pv_issued = 0;
+      uint32_t kv_count = 0, q_count = 0, issued = 0;
       const uint32_t qx = smem_addr(sQ + x * C::kQTileBytes);
       for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
         const Item it = decode_item(P, item);
-        if (!mbar_wait(q_full, q_count & 1, abort_flag, a.status)) break;
-        ++q_count;
-        tc_fence_after();
+        if (!pv_role) {
+          if (!mbar_wait(q_full, q_count & 1, abort_flag, a.status)) break;
+          ++q_count;
+          tc_fence_after();
+        }
         bool first_pv = true;
-        for (int j = 0; j <= it.n_tiles; ++j) {
-          if (j < it.n_tiles) {
-            const uint32_t kc = kv_count + j;
-            const int st = kc % NS;
+        for (int j = 0; j < it.n_tiles; ++j) {
+          // Stage arrivals are parity waits, exact only within one phase.  A
+          // score thread observes every stage in order and releases the
+          // tiles outside its band itself; the P V thread releases the
+          // others after their P V and waits only on those, when score tile
+          // n has already observed the arrival.  So no stage is refilled
+          // before both threads of a query tile have seen its last fill.
+          const uint32_t kc = kv_count + j;
+          const int st = kc % NS;
+          const bool relevant = tile_relevant(P, it, x, (it.kt_hi - j) * BKV);
+          if (!pv_role || relevant) {
             if (!mbar_wait(&kv_full[st], (kc / NS) & 1, abort_flag, a.status)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            if (tile_relevant(P, it, x, (it.kt_hi - j) * BKV)) {
+          }
+          const uint32_t n = issued;
+          if (!pv_role) {
+            if (relevant) {
               // Score buffer n % 2 still holds P number n - 2 until its P V ends.
-              const uint32_t n = s_issued;
               if (n >= 2) {
                 if (!mbar_wait(&pv_done[2 * x + (n & 1)], ((n - 2) >> 1) & 1, abort_flag,
                                a.status)) {
@@ -268,43 +282,46 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
                              sw128_kmajor_desc(k_addr + at * BKV * 128 + off), idesc_s, kk > 0);
               }
               umma_commit(&s_full[2 * x + (n & 1)]);
-              ++s_issued;
+              ++issued;
             } else {
-              umma_commit(&kv_empty[st]);  // this query tile never reads the stage
+              mbar_arrive(&kv_empty[st]);  // this query tile never reads the stage
             }
             if (j == it.n_tiles - 1) umma_commit(q_empty);  // Q_X is free once these finish
-          }
-          if (j >= 1 && tile_relevant(P, it, x, (it.kt_hi - (j - 1)) * BKV)) {
-            const int st = (kv_count + j - 1) % NS;
-            const uint32_t n = pv_issued;  // P number n sits in score buffer n % 2
-            if (!mbar_wait(&p_full[2 * x + (n & 1)], (n >> 1) & 1, abort_flag, a.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t p_tmem = tmem + C::s_col(x, n & 1);
-            const uint32_t d_tmem = tmem + C::o_col(x);
-            const uint32_t v_addr = smem_addr(sV + st * C::kKVBytes);
+          } else {
+            if (relevant) {
+              // P number n sits in score buffer n % 2.  Score tile n was read
+              // by then, so this P V also follows every score MMA of the stage
+              // by this query tile.
+              if (!mbar_wait(&p_full[2 * x + (n & 1)], (n >> 1) & 1, abort_flag, a.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t p_tmem = tmem + C::s_col(x, n & 1);
+              const uint32_t d_tmem = tmem + C::o_col(x);
+              const uint32_t v_addr = smem_addr(sV + st * C::kKVBytes);
 #pragma unroll
-            for (int kk = 0; kk < BKV / 16; ++kk)  // 16 keys = 8 packed P columns
-              umma_bf16_ts(d_tmem, p_tmem + kk * 8,
-                           sw128_mnmajor_desc(v_addr + kk * 16 * 128, BKV * 128), idesc_pv,
-                           (!first_pv || kk > 0) ? 1u : 0u);
-            umma_commit(&pv_done[2 * x + (n & 1)]);
-            umma_commit(&kv_empty[st]);
-            ++pv_issued;
-            first_pv = false;
+              for (int kk = 0; kk < BKV / 16; ++kk)  // 16 keys = 8 packed P columns
+                umma_bf16_ts(d_tmem, p_tmem + kk * 8,
+                             sw128_mnmajor_desc(v_addr + kk * 16 * 128, BKV * 128), idesc_pv,
+                             (!first_pv || kk > 0) ? 1u : 0u);
+              umma_commit(&pv_done[2 * x + (n & 1)]);
+              umma_commit(&kv_empty[st]);  // this query tile is done with the stage
+              ++issued;
+              first_pv = false;
+            }
           }
         }
         kv_count += it.n_tiles;
       }
-      umma_commit(&done_bar[x]);
+      const int me = pv_role ? QT + x : x;
+      umma_commit(&done_bar[me]);
       volatile int no_abort = 0;
-      mbar_wait(&done_bar[x], 0, &no_abort, a.status);
+      mbar_wait(&done_bar[me], 0, &no_abort, a.status);
     }
   } else {
     // --------------------------------------------------------- softmax --
-    const int x = (warp - 1 - QT) >> 2;  // query tile of this warpgroup
+    const int x = (warp - 1 - 2 * QT) >> 2;  // query tile of this warpgroup
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row in the query tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
