@@ -111,6 +111,21 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok);
 }
 
+// ------------------------------------------------------- work schedule --
+
+// Work item number k of this CTA when items sorted longest first are dealt
+// to the gridDim.x CTAs of a persistent kernel in snake order: even rounds
+// go to the CTAs in increasing order, odd rounds in decreasing order, so
+// the CTA that got a round's longest item gets the next round's shortest.
+// Round-robin dealing leaves the first CTAs with every round's longest item
+// (up to 1.2x the mean load on the attention shapes here; snake order
+// 1.05-1.1x).
+__device__ __forceinline__ int snake_item(int k) {
+  const int c = (k & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                        : static_cast<int>(blockIdx.x);
+  return k * static_cast<int>(gridDim.x) + c;
+}
+
 // ------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -86,7 +86,8 @@ struct Item {
 };
 
 // kKV: key blocks in increasing order (most query tiles first); kQ: query
-// blocks in decreasing order (most key tiles first).
+// blocks in decreasing order (most key tiles first).  Either way the items
+// run longest first and are dealt to the CTAs in snake order (snake_item).
 template <int MODE>
 __device__ __forceinline__ Item decode_item(const BwdParams& P, int item) {
   Item it;
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
       bool ok = true;
       uint32_t mv_count = 0, stat_count = 0;
       uint32_t armed = 0, armed_parity = 0;
-      for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
+      for (int k = 0, item = snake_item(0); ok && item < P.num_items; item = snake_item(++k)) {
         const Item it = decode_item<MODE>(P, item);
         if (!mbar_wait(stat_empty, (stat_count & 1) ^ 1u, abort_flag, a.status)) {
           ok = false;
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
       bool ok = true;
       uint32_t mv_count = 0, stat_count = 0, s_issued = 0, op_issued = 0, items_done = 0;
       const uint32_t stat0 = smem_addr(sStat), stat1 = stat0 + C::kStatBytes;
-      for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
+      for (int k = 0, item = snake_item(0); ok && item < P.num_items; item = snake_item(++k)) {
         const Item it = decode_item<MODE>(P, item);
         if (!mbar_wait(stat_full, stat_count & 1, abort_flag, a.status)) break;
         ++stat_count;
@@ -376,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
       tc_fence_after();
       return true;
     };
-    for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
+    for (int k = 0, item = snake_item(0); ok && item < P.num_items; item = snake_item(++k)) {
       const Item it = decode_item<MODE>(P, item);
       const int row = it.r0 + r;  // this thread's stationary position
       const int64_t bh = static_cast<int64_t>(it.b) * a.heads + it.h;
@@ -591,7 +592,7 @@ cudaError_t launch_swa_backward(const SwaBwdArgs& a, cudaStream_t stream) {
   prm.a = a;
   prm.blocks = (a.seq + BR - 1) / BR;
   const int64_t items = static_cast<int64_t>(prm.blocks) * a.heads * a.batch;
-  if (items > 0x7fffffff) return cudaErrorInvalidValue;
+  if (items > 0x3fffffff) return cudaErrorInvalidValue;  // item numbers stay in int
   prm.num_items = static_cast<int>(items);
   const int grid = static_cast<int>(items < a.sms ? items : a.sms);
   int sd[4];

@@ -88,8 +88,8 @@ struct Item {
   int q0, h, b, kt_hi, n_tiles;
 };
 
-// Items are ordered by query block, last (most key tiles) first, so the
-// round-robin split over CTAs hands out the long items before the short ones.
+// Items are ordered by query block, last (most key tiles) first, and dealt
+// to the CTAs in snake order (snake_item), which evens out the per-CTA work.
 __device__ __forceinline__ Item decode_item(const SwaParams& P, int item) {
   Item it;
   const int per_block = P.a.heads * P.a.batch;
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
       bool ok = true;
       uint32_t kv_count = 0, q_count = 0;
       uint32_t armed = 0, armed_parity = 0;
-      for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
+      for (int k = 0, item = snake_item(0); ok && item < P.num_items; item = snake_item(++k)) {
         const Item it = decode_item(P, item);
         if (!mbar_wait(q_empty, (q_count & 1) ^ 1u, abort_flag, a.status)) {
           ok = false;
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
       bool ok = true;
       uint32_t kv_count = 0, q_count = 0, issued = 0;
       const uint32_t qx = smem_addr(sQ + x * C::kQTileBytes);
-      for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
+      for (int k = 0, item = snake_item(0); ok && item < P.num_items; item = snake_item(++k)) {
         const Item it = decode_item(P, item);
         if (!pv_role) {
           if (!mbar_wait(q_full, q_count & 1, abort_flag, a.status)) break;
@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
       return true;
     };
 
-    for (int item = blockIdx.x; ok && item < P.num_items; item += gridDim.x) {
+    for (int k = 0, item = snake_item(0); ok && item < P.num_items; item = snake_item(++k)) {
       const Item it = decode_item(P, item);
       const int i = it.q0 + x * BQ + r;  // query position of this thread
       if (it.q0 + x * BQ >= a.seq) continue;
@@ -569,7 +569,7 @@ cudaError_t launch_swa(const SwaArgs& a, cudaStream_t stream) {
   prm.seq_dim = sd_q;
   prm.q_blocks = (a.seq + QT * BQ - 1) / (QT * BQ);
   const int64_t items = static_cast<int64_t>(prm.q_blocks) * a.heads * a.batch;
-  if (items > 0x7fffffff) return cudaErrorInvalidValue;
+  if (items > 0x3fffffff) return cudaErrorInvalidValue;  // item numbers stay in int
   prm.num_items = static_cast<int>(items);
   const int grid = static_cast<int>(items < a.sms ? items : a.sms);
   return a.counts ? dispatch<true>(prm, grid, stream) : dispatch<false>(prm, grid, stream);
