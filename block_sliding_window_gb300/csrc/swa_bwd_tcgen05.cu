@@ -18,8 +18,9 @@
 //   kQ   one item = 128 queries: stationary Q and dO, moving 64-key tiles
 //          S = Q K^T,  dP = dO V^T            (M 128 queries, N 64, K d)
 //          dQ += dS K                         (M 128, N d, K 64 keys)
-// Roles (320 threads): warp 0 TMA, warp 1 TMEM owner and MMA issuer, warps
-// 2..9 two warpgroups; warp w serves the stationary rows of TMEM lane
+// Roles (384 threads): warp 0 TMA; warps 1, 2, 3 issue the S, dP and
+// accumulate MMAs (one thread each; warp 1 owns TMEM); warps 4..11 two
+// warpgroups; warp w serves the stationary rows of TMEM lane
 // quarter w % 4 (one row per thread) and the tile's columns 32 * g .. +31 of
 // its warpgroup g: recompute P and dS for them in fp32, write them as bf16
 // operand half-rows into shared memory (128-byte-swizzled K-major layout, one
@@ -37,7 +38,7 @@ namespace {
 
 constexpr int BR = 128;  // stationary rows per item (= MMA M)
 constexpr int BC = 64;   // moving rows per tile (= N of the score MMAs)
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kGroupCols = BC / 2;  // moving columns per softmax warpgroup
 constexpr int kKV = 0;   // dK, dV kernel
 constexpr int kQ = 1;    // dQ kernel
@@ -174,10 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
   uint64_t* s_full = mv_empty + NS;     // [2]
   uint64_t* p_full = s_full + 2;        // [2]
   uint64_t* op_done = p_full + 2;       // [2]
-  uint64_t* acc_full = op_done + 2;
+  uint64_t* s_read = op_done + 2;       // [2]: score buffer 0 / 1 read out of TMEM
+  uint64_t* acc_full = s_read + 2;
   uint64_t* acc_empty = acc_full + 1;
-  uint64_t* done_bar = acc_empty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* done_bar = acc_empty + 1;   // [3]: one per issuing thread
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -185,19 +187,20 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
     mbar_init(stat_full, 1);
-    mbar_init(stat_empty, 1);
+    mbar_init(stat_empty, 2);  // the S and dP threads release the stationary tiles
     for (int s = 0; s < NS; ++s) {
       mbar_init(&mv_full[s], 1);
       mbar_init(&mv_empty[s], 1);
     }
     for (int k = 0; k < 2; ++k) {
-      mbar_init(&s_full[k], 1);
+      mbar_init(&s_full[k], 2);  // S and dP of one buffer, from two threads
       mbar_init(&p_full[k], 8);
       mbar_init(&op_done[k], 1);
+      mbar_init(&s_read[k], 8);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 8);
-    mbar_init(done_bar, 1);
+    for (int k = 0; k < 3; ++k) mbar_init(&done_bar[k], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -265,59 +268,68 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
           mbar_wait(&mv_full[s], (armed_parity >> s) & 1u, &no_abort, a.status);
       if (stat_count > 0) mbar_wait(stat_full, (stat_count - 1) & 1, &no_abort, a.status);
     }
-  } else if (warp == 1) {
+  } else if (warp <= 3) {
     // ------------------------------------------------------------- MMA --
+    // Three issuing threads: warp 1 the S scores, warp 2 the dP scores,
+    // warp 3 the accumulate MMAs.  One thread issues at most one tcgen05
+    // instruction (MMA or commit) every ~75 cycles whatever the MMA's N,
+    // slower than the tensor pipe runs these N = 64 MMAs; three streams keep
+    // it fed.  All three observe every moving stage in order.  The stage is
+    // released by the accumulate thread after the tile's accumulate MMAs,
+    // which follow the tile's score MMAs (those were read before P / dS was
+    // written), so no stage is refilled before all three have seen it.
+    const int role = warp - 1;  // 0: S, 1: dP, 2: accumulate
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16(BR, BC);
       constexpr uint32_t idesc_acc = umma_idesc_bf16(BR, D) | (1u << 16);  // B MN-major
       bool ok = true;
-      uint32_t mv_count = 0, stat_count = 0, s_issued = 0, op_issued = 0, items_done = 0;
-      const uint32_t stat0 = smem_addr(sStat), stat1 = stat0 + C::kStatBytes;
+      uint32_t mv_count = 0, stat_count = 0, issued = 0, items_done = 0;
+      const uint32_t stat = smem_addr(sStat) + (role == 1 ? C::kStatBytes : 0);
       for (int k = 0, item = snake_item(0); ok && item < P.num_items; item = snake_item(++k)) {
         const Item it = decode_item<MODE>(P, item);
-        if (!mbar_wait(stat_full, stat_count & 1, abort_flag, a.status)) break;
-        ++stat_count;
-        tc_fence_after();
-        for (int j = 0; ok && j <= it.n_tiles; ++j) {
-          if (j < it.n_tiles) {
-            const uint32_t mc = mv_count + j;
-            const int st = mc % NS;
-            if (!mbar_wait(&mv_full[st], (mc / NS) & 1, abort_flag, a.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t mv0 = smem_addr(sMv + st * 2 * C::kMvBytes), mv1 = mv0 + C::kMvBytes;
-            const int buf = s_issued & 1;
-            // Scores of stationary rows against the moving tile:
-            //   kKV: S^T = K Q^T, dP^T = V dO^T;  kQ: S = Q K^T, dP = dO V^T.
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t at = kk / 4, off = (kk % 4) * 32;
-              umma_bf16_ss(tmem + C::s_col(buf), sw128_kmajor_desc(stat0 + at * BR * 128 + off),
-                           sw128_kmajor_desc(mv0 + at * BC * 128 + off), idesc_s, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t at = kk / 4, off = (kk % 4) * 32;
-              umma_bf16_ss(tmem + C::dp_col(buf), sw128_kmajor_desc(stat1 + at * BR * 128 + off),
-                           sw128_kmajor_desc(mv1 + at * BC * 128 + off), idesc_s, kk > 0);
-            }
-            umma_commit(&s_full[buf]);
-            ++s_issued;
-            if (j == it.n_tiles - 1) umma_commit(stat_empty);  // stationary tiles are free
+        if (role < 2) {
+          if (!mbar_wait(stat_full, stat_count & 1, abort_flag, a.status)) break;
+          ++stat_count;
+          tc_fence_after();
+        }
+        for (int j = 0; j < it.n_tiles; ++j) {
+          const uint32_t mc = mv_count + j;
+          const int st = mc % NS;
+          if (!mbar_wait(&mv_full[st], (mc / NS) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
           }
-          if (j >= 1) {
-            const uint32_t mc = mv_count + j - 1;
-            const int st = mc % NS;
-            const uint32_t mv0 = smem_addr(sMv + st * 2 * C::kMvBytes), mv1 = mv0 + C::kMvBytes;
-            const uint32_t n = op_issued;  // operand buffer n % kOpBufs
+          tc_fence_after();
+          const uint32_t mv0 = smem_addr(sMv + st * 2 * C::kMvBytes), mv1 = mv0 + C::kMvBytes;
+          const uint32_t n = issued;
+          if (role < 2) {
+            // Scores of the stationary rows against the moving tile:
+            //   kKV: S^T = K Q^T, dP^T = V dO^T;  kQ: S = Q K^T, dP = dO V^T.
+            // Buffer n % 2 is free once score tile n - 2 has been read.
+            if (n >= 2) {
+              if (!mbar_wait(&s_read[n & 1], ((n - 2) >> 1) & 1, abort_flag, a.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint32_t mv = role == 0 ? mv0 : mv1;
+            const uint32_t d_tmem = tmem + (role == 0 ? C::s_col(n & 1) : C::dp_col(n & 1));
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t at = kk / 4, off = (kk % 4) * 32;
+              umma_bf16_ss(d_tmem, sw128_kmajor_desc(stat + at * BR * 128 + off),
+                           sw128_kmajor_desc(mv + at * BC * 128 + off), idesc_s, kk > 0);
+            }
+            umma_commit(&s_full[n & 1]);
+            if (j == it.n_tiles - 1) umma_commit(stat_empty);  // stationary tiles are free
+          } else {
             const uint32_t ob = n % C::kOpBufs, oph = (n / C::kOpBufs) & 1;
             if (!mbar_wait(&p_full[ob], oph, abort_flag, a.status)) {
               ok = false;
               break;
             }
-            if (j == 1) {  // the accumulators of the previous item have been read out
+            if (j == 0) {  // the accumulators of the previous item have been read out
               if (!mbar_wait(acc_empty, (items_done & 1) ^ 1u, abort_flag, a.status)) {
                 ok = false;
                 break;
@@ -325,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
             }
             tc_fence_after();
             const uint32_t op = smem_addr(sOp + ob * C::kNOps * C::kOpRowBytes);
-            const bool first = j == 1;
+            const bool first = j == 0;
             // The moving tile as the MN-major B operand: rows = its 64
             // positions (K), 64-column blocks of d (N) 64 * 128 bytes apart.
             if constexpr (MODE == kKV) {
@@ -350,25 +362,27 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
             }
             umma_commit(&op_done[ob]);
             umma_commit(&mv_empty[st]);
-            ++op_issued;
           }
+          ++issued;
         }
         if (!ok) break;
-        umma_commit(acc_full);
-        ++items_done;
+        if (role == 2) {
+          umma_commit(acc_full);
+          ++items_done;
+        }
         mv_count += it.n_tiles;
       }
-      umma_commit(done_bar);
+      umma_commit(&done_bar[role]);
       volatile int no_abort = 0;
-      mbar_wait(done_bar, 0, &no_abort, a.status);
+      mbar_wait(&done_bar[role], 0, &no_abort, a.status);
     }
   } else {
     // ------------------------------------------------- P, dS and output --
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // stationary row = TMEM lane
-    const int grp = (warp - 2) >> 2;    // this warpgroup's columns: 32 * grp .. +31
+    const int grp = (warp - 4) >> 2;    // this warpgroup's columns: 32 * grp .. +31
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    float* wl = sLse + (warp - 2) * 2 * kGroupCols;  // this warp's lse / delta staging (kKV)
+    float* wl = sLse + (warp - 4) * 2 * kGroupCols;  // this warp's lse / delta staging (kKV)
     uint32_t seen = 0, items_done = 0;
     bool ok = true;
     auto wait_op = [&](uint32_t n) -> bool {  // operand buffer n % kOpBufs free again
@@ -406,6 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
         tmem_ld_32x32b_x32(tmem + lane_base + C::s_col(buf) + grp * kGroupCols, s_raw);
         tmem_ld_32x32b_x32(tmem + lane_base + C::dp_col(buf) + grp * kGroupCols, dp_raw);
         tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_read[buf]);  // the buffer may take score tile seen + 2
         float s[kGroupCols], dp[kGroupCols];
 #pragma unroll
         for (int e = 0; e < kGroupCols; ++e) {
