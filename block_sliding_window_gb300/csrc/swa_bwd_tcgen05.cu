@@ -22,10 +22,14 @@
 // accumulate MMAs (one thread each; warp 1 owns TMEM); warps 4..11 two
 // warpgroups; warp w serves the stationary rows of TMEM lane
 // quarter w % 4 (one row per thread) and the tile's columns 32 * g .. +31 of
-// its warpgroup g: recompute P and dS for them in fp32, write them as bf16
-// operand half-rows into shared memory (128-byte-swizzled K-major layout, one
-// buffer), and at the end of an item read the fp32 accumulators from TMEM
-// and store bf16 gradients.  (With one warpgroup doing all 64 columns the
+// its warpgroup g: recompute P and dS for them in fp32 and write them as
+// bf16 back into TMEM over the first half of those score columns (two
+// positions per column), where the accumulate MMAs read them as their A
+// operand: the stationary rows are the TMEM lanes in both kernels, so P^T and
+// dS^T (kKV) or dS (kQ) are lane-major as they stand.  A score buffer takes
+// tile n + 2 once the accumulate MMAs of tile n have finished.  At the end of
+// an item the warps read the fp32 accumulators from TMEM and store bf16
+// gradients.  (With one warpgroup doing all 64 columns the
 // kernels ran at 14-19% tensor activity, ~6k / 3.5k cycles per tile.)  The
 // moving tiles are read twice, once as K-major and once as MN-major operands
 // of the same shared-memory copy.
@@ -48,23 +52,22 @@ struct BwdCfg {
   static constexpr int kAtoms = (D + 63) / 64;
   static constexpr int kStatBytes = kAtoms * BR * 128;  // one stationary operand
   static constexpr int kMvBytes = kAtoms * BC * 128;    // one moving operand, one stage
-  // One operand buffer (the accumulate MMAs of a tile are short, so the
-  // rows of the next tile rarely wait for them) leaves room for more stages
-  // of moving tiles, which is what these latency-bound kernels need.
-  static constexpr int kOpBufs = 1;
-  static constexpr int kOpRowBytes = BR * 128;          // one P / dS operand buffer
-  static constexpr int kNOps = MODE == kKV ? 2 : 1;      // P^T and dS^T, or dS
-  static constexpr int kStageLse = 8 * 2 * kGroupCols * 4;  // per-warp lse / delta (kKV)
-  static constexpr int kFixed = 2 * kStatBytes + kOpBufs * kNOps * kOpRowBytes + kStageLse +
-                                512 + 1024;
+  // P^T / dS^T (or dS) never touch shared memory: they overwrite their own
+  // score columns in TMEM, so shared memory holds only the stationary tiles
+  // and the ring of moving tiles.
+  static constexpr int kStageLse = MODE == kKV ? 8 * 2 * kGroupCols * 4 : 0;  // lse / delta
+  static constexpr int kFixed = 2 * kStatBytes + kStageLse + 512 + 1024;
   static constexpr int kNSFit = (227 * 1024 - kFixed) / (2 * kMvBytes);
   static constexpr int kNS = kNSFit < 6 ? kNSFit : 6;   // moving stages
   static constexpr int kSmemBytes = kFixed + kNS * 2 * kMvBytes;
   static constexpr int kTmemCols = 512;
   // Score buffers: S at buf * 128, dP at buf * 128 + 64; accumulators after.
+  // Warpgroup g's 32 columns of a score buffer take its 16 packed bf16
+  // columns of P (or dS) in their first half: p_col(g) from the buffer.
   __host__ __device__ static constexpr int s_col(int buf) { return buf * 128; }
   __host__ __device__ static constexpr int dp_col(int buf) { return buf * 128 + 64; }
   __host__ __device__ static constexpr int acc_col(int i) { return 256 + i * D; }
+  __host__ __device__ static constexpr int p_col(int g) { return g * kGroupCols; }
 };
 
 struct BwdParams {
@@ -142,19 +145,6 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float (
                    pack_bf16x2(v[e + 6] * mul, v[e + 7] * mul));
 }
 
-// 32 bf16 values (64 bytes: 16-byte chunks 4g .. 4g + 3 of the row) into row
-// r of a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ void store_op_half(uint8_t* tile, int r, int g,
-                                              const uint32_t (&pk)[16]) {
-  uint8_t* row = tile + r * 128;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int c = 4 * g + j;
-    *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
-        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-  }
-}
-
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_constant__ BwdParams P) {
   using C = BwdCfg<D, MODE>;
@@ -165,8 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sStat = smem;                               // [2][kStatBytes]
   uint8_t* sMv = sStat + 2 * C::kStatBytes;            // [NS][2][kMvBytes]
-  uint8_t* sOp = sMv + NS * 2 * C::kMvBytes;           // [kOpBufs][kNOps][kOpRowBytes]
-  float* sLse = reinterpret_cast<float*>(sOp + C::kOpBufs * C::kNOps * C::kOpRowBytes);
+  float* sLse = reinterpret_cast<float*>(sMv + NS * 2 * C::kMvBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sLse) + C::kStageLse);
   uint64_t* stat_full = bars;
   uint64_t* stat_empty = stat_full + 1;
@@ -174,9 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
   uint64_t* mv_empty = mv_full + NS;    // [NS]
   uint64_t* s_full = mv_empty + NS;     // [2]
   uint64_t* p_full = s_full + 2;        // [2]
-  uint64_t* op_done = p_full + 2;       // [2]
-  uint64_t* s_read = op_done + 2;       // [2]: score buffer 0 / 1 read out of TMEM
-  uint64_t* acc_full = s_read + 2;
+  uint64_t* acc_done = p_full + 2;      // [2]: accumulate MMAs of buffer 0 / 1 done
+  uint64_t* acc_full = acc_done + 2;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* done_bar = acc_empty + 1;   // [3]: one per issuing thread
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 3);
@@ -195,8 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
     for (int k = 0; k < 2; ++k) {
       mbar_init(&s_full[k], 2);  // S and dP of one buffer, from two threads
       mbar_init(&p_full[k], 8);
-      mbar_init(&op_done[k], 1);
-      mbar_init(&s_read[k], 8);
+      mbar_init(&acc_done[k], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 8);
@@ -305,9 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
           if (role < 2) {
             // Scores of the stationary rows against the moving tile:
             //   kKV: S^T = K Q^T, dP^T = V dO^T;  kQ: S = Q K^T, dP = dO V^T.
-            // Buffer n % 2 is free once score tile n - 2 has been read.
+            // Buffer n % 2 holds P / dS of tile n - 2 until its accumulate
+            // MMAs have finished.
             if (n >= 2) {
-              if (!mbar_wait(&s_read[n & 1], ((n - 2) >> 1) & 1, abort_flag, a.status)) {
+              if (!mbar_wait(&acc_done[n & 1], ((n - 2) >> 1) & 1, abort_flag, a.status)) {
                 ok = false;
                 break;
               }
@@ -324,8 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
             umma_commit(&s_full[n & 1]);
             if (j == it.n_tiles - 1) umma_commit(stat_empty);  // stationary tiles are free
           } else {
-            const uint32_t ob = n % C::kOpBufs, oph = (n / C::kOpBufs) & 1;
-            if (!mbar_wait(&p_full[ob], oph, abort_flag, a.status)) {
+            if (!mbar_wait(&p_full[n & 1], (n >> 1) & 1, abort_flag, a.status)) {
               ok = false;
               break;
             }
@@ -336,31 +323,36 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
               }
             }
             tc_fence_after();
-            const uint32_t op = smem_addr(sOp + ob * C::kNOps * C::kOpRowBytes);
             const bool first = j == 0;
-            // The moving tile as the MN-major B operand: rows = its 64
-            // positions (K), 64-column blocks of d (N) 64 * 128 bytes apart.
+            // A from TMEM: 16 moving positions = 8 packed columns, those of
+            // warpgroup kk / 2 (positions 32 * (kk / 2) ..) in its half of the
+            // score buffer.  B: the moving tile as the MN-major operand, rows
+            // = its 64 positions (K), 64-column blocks of d (N) 64 * 128
+            // bytes apart.
+            auto a_col = [&](int base, int kk) {
+              return tmem + base + C::p_col(kk >> 1) + (kk & 1) * 8;
+            };
             if constexpr (MODE == kKV) {
               // dV += P^T dO, dK += dS^T Q
 #pragma unroll
               for (int kk = 0; kk < BC / 16; ++kk)
-                umma_bf16_ss(tmem + C::acc_col(0), sw128_kmajor_desc(op + kk * 32),
+                umma_bf16_ts(tmem + C::acc_col(0), a_col(C::s_col(n & 1), kk),
                              sw128_mnmajor_desc(mv1 + kk * 16 * 128, BC * 128), idesc_acc,
                              (!first || kk > 0) ? 1u : 0u);
 #pragma unroll
               for (int kk = 0; kk < BC / 16; ++kk)
-                umma_bf16_ss(tmem + C::acc_col(1), sw128_kmajor_desc(op + C::kOpRowBytes + kk * 32),
+                umma_bf16_ts(tmem + C::acc_col(1), a_col(C::dp_col(n & 1), kk),
                              sw128_mnmajor_desc(mv0 + kk * 16 * 128, BC * 128), idesc_acc,
                              (!first || kk > 0) ? 1u : 0u);
             } else {
               // dQ += dS K
 #pragma unroll
               for (int kk = 0; kk < BC / 16; ++kk)
-                umma_bf16_ss(tmem + C::acc_col(0), sw128_kmajor_desc(op + kk * 32),
+                umma_bf16_ts(tmem + C::acc_col(0), a_col(C::dp_col(n & 1), kk),
                              sw128_mnmajor_desc(mv0 + kk * 16 * 128, BC * 128), idesc_acc,
                              (!first || kk > 0) ? 1u : 0u);
             }
-            umma_commit(&op_done[ob]);
+            umma_commit(&acc_done[n & 1]);
             umma_commit(&mv_empty[st]);
           }
           ++issued;
@@ -385,12 +377,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
     float* wl = sLse + (warp - 4) * 2 * kGroupCols;  // this warp's lse / delta staging (kKV)
     uint32_t seen = 0, items_done = 0;
     bool ok = true;
-    auto wait_op = [&](uint32_t n) -> bool {  // operand buffer n % kOpBufs free again
-      if (!mbar_wait_warp(&op_done[n % C::kOpBufs], (n / C::kOpBufs) & 1, abort_flag, a.status))
-        return false;
-      tc_fence_after();
-      return true;
-    };
     for (int k = 0, item = snake_item(0); ok && item < P.num_items; item = snake_item(++k)) {
       const Item it = decode_item<MODE>(P, item);
       const int row = it.r0 + r;  // this thread's stationary position
@@ -420,9 +406,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
         tmem_ld_32x32b_x32(tmem + lane_base + C::s_col(buf) + grp * kGroupCols, s_raw);
         tmem_ld_32x32b_x32(tmem + lane_base + C::dp_col(buf) + grp * kGroupCols, dp_raw);
         tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_read[buf]);  // the buffer may take score tile seen + 2
         float s[kGroupCols], dp[kGroupCols];
 #pragma unroll
         for (int e = 0; e < kGroupCols; ++e) {
@@ -449,24 +432,15 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
           pk_p[e / 2] = pack_bf16x2(pv[0], pv[1]);
           pk_ds[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
         }
-        // The operand buffer was last read by the accumulate MMAs of tile
-        // seen - kOpBufs.
-        if (seen >= static_cast<uint32_t>(C::kOpBufs) && !wait_op(seen - C::kOpBufs)) {
-          ok = false;
-          break;
-        }
-        const int ob = static_cast<int>(seen % C::kOpBufs);
-        uint8_t* ops = sOp + ob * C::kNOps * C::kOpRowBytes;
-        if constexpr (MODE == kKV) {
-          store_op_half(ops, r, grp, pk_p);
-          store_op_half(ops + C::kOpRowBytes, r, grp, pk_ds);
-        } else {
-          store_op_half(ops, r, grp, pk_ds);
-        }
-        fence_proxy_async_smem();
+        // P^T and dS^T (kKV) or dS (kQ) over the first half of this
+        // warpgroup's score columns, which it has just read.
+        if constexpr (MODE == kKV)
+          tmem_st_32x32b_x16(tmem + lane_base + C::s_col(buf) + C::p_col(grp), pk_p);
+        tmem_st_32x32b_x16(tmem + lane_base + C::dp_col(buf) + C::p_col(grp), pk_ds);
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[ob]);
+        if (lane == 0) mbar_arrive(&p_full[buf]);
         ++seen;
       }
       if (!ok) break;
