@@ -381,9 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
       const Item it = decode_item<MODE>(P, item);
       const int row = it.r0 + r;  // this thread's stationary position
       const int64_t bh = static_cast<int64_t>(it.b) * a.heads + it.h;
-      float lse_row = 0.f, delta_row = 0.f;
+      float nlse_row = 0.f, delta_row = 0.f;  // -lse, so the exponent is one FMA
       if (MODE == kQ && row < a.seq) {
-        lse_row = a.lse[bh * a.seq + row];
+        nlse_row = -a.lse[bh * a.seq + row];
         delta_row = a.delta[bh * a.seq + row];
       }
       for (int t = 0; t < it.n_tiles; ++t) {
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
         if (MODE == kKV) {  // per-query lse and delta of the columns, staged per warp
           __syncwarp();
           const int q = c0 + lane;
-          wl[lane] = q < a.seq ? a.lse[bh * a.seq + q] : 0.f;
+          wl[lane] = q < a.seq ? -a.lse[bh * a.seq + q] : 0.f;  // negated: one FMA below
           wl[kGroupCols + lane] = q < a.seq ? a.delta[bh * a.seq + q] : 0.f;
           __syncwarp();
         }
@@ -412,25 +412,53 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
           s[e] = __uint_as_float(s_raw[e]);
           dp[e] = __uint_as_float(dp_raw[e]);
         }
+        // Moving positions c0 + e with e in [lo, hi] are in the band of this
+        // thread's row (kKV: queries row .. row + w - 1 that exist; kQ: keys
+        // row - w + 1 .. row); a tile wholly inside it skips the mask.
+        const int w = min(a.window, a.seq);  // no int overflow for any window
+        const int lo = MODE == kKV ? row - c0 : row - w + 1 - c0;
+        const int hi = row >= a.seq ? -1
+                       : MODE == kKV ? min(row + w - 1, a.seq - 1) - c0 : row - c0;
+        const bool interior = lo <= 0 && hi >= kGroupCols - 1;
+        float nl2v[kGroupCols], dlv[kGroupCols];
+        if constexpr (MODE == kKV) {  // per-query -lse and delta of the columns
+#pragma unroll
+          for (int e = 0; e < kGroupCols; e += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(wl + e);
+            const float4 d4 = *reinterpret_cast<const float4*>(wl + kGroupCols + e);
+            nl2v[e] = l4.x; nl2v[e + 1] = l4.y; nl2v[e + 2] = l4.z; nl2v[e + 3] = l4.w;
+            dlv[e] = d4.x; dlv[e + 1] = d4.y; dlv[e + 2] = d4.z; dlv[e + 3] = d4.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < kGroupCols; ++e) {
+            nl2v[e] = nlse_row;
+            dlv[e] = delta_row;
+          }
+        }
+        // Packed f32x2 arithmetic, two moving positions per instruction:
+        // these warps are bound by instruction issue.
+        const uint64_t scale2 = f2(a.scale_log2, a.scale_log2);
+        float pv[kGroupCols];
+#pragma unroll
+        for (int e = 0; e < kGroupCols; e += 2) {
+          float t0, t1;
+          f2_split(f2_fma(f2(s[e], s[e + 1]), scale2, f2(nl2v[e], nl2v[e + 1])), t0, t1);
+          pv[e] = fast_exp2(t0);
+          pv[e + 1] = fast_exp2(t1);
+        }
+        if (!interior) {
+#pragma unroll
+          for (int e = 0; e < kGroupCols; ++e) pv[e] = (e >= lo && e <= hi) ? pv[e] : 0.f;
+        }
         uint32_t pk_p[kGroupCols / 2], pk_ds[kGroupCols / 2];
 #pragma unroll
         for (int e = 0; e < kGroupCols; e += 2) {
-          float pv[2], dsv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = c0 + e + u;  // moving position
-            // kKV: key `row`, query c;  kQ: query `row`, key c.
-            const int qi = MODE == kKV ? c : row;
-            const int kj = MODE == kKV ? row : c;
-            const bool vis = kj <= qi && qi - kj < a.window && qi < a.seq && kj < a.seq;
-            const float l2 = MODE == kKV ? wl[e + u] : lse_row;
-            const float dl = MODE == kKV ? wl[kGroupCols + e + u] : delta_row;
-            const float p = vis ? fast_exp2(s[e + u] * a.scale_log2 - l2) : 0.f;
-            pv[u] = p;
-            dsv[u] = p * (dp[e + u] - dl);
-          }
-          pk_p[e / 2] = pack_bf16x2(pv[0], pv[1]);
-          pk_ds[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
+          float d0, d1;
+          f2_split(f2_mul(f2(pv[e], pv[e + 1]),
+                          f2_sub(f2(dp[e], dp[e + 1]), f2(dlv[e], dlv[e + 1]))), d0, d1);
+          pk_p[e / 2] = pack_bf16x2(pv[e], pv[e + 1]);
+          pk_ds[e / 2] = pack_bf16x2(d0, d1);
         }
         // P^T and dS^T (kKV) or dS (kQ) over the first half of this
         // warpgroup's score columns, which it has just read.

@@ -386,9 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
         } else if (COUNTS) {
           cnt += BKV;
         }
+        // Packed forms keep the per-score instruction count low: one
+        // three-input max per two scores, one f32x2 FMA (scale, shift) and
+        // one f32x2 add (row sum) per pair; the softmax warps are bound by
+        // instruction issue, not by the exponent unit.
         float mx = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < BKV; ++e) mx = fmaxf(mx, v[e]);
+        for (int e = 0; e < BKV; e += 2) mx = fmax3(mx, v[e], v[e + 1]);
         mx *= a.scale_log2;  // row max in the log2 domain
         // Raise the reference max only when the row max passes it by 2^8.
         float alpha = 1.f;
@@ -399,16 +403,20 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
           m_ref = mx;
         }
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        float rs = 0.f;
+        const uint64_t scale2 = f2(a.scale_log2, a.scale_log2), shift2 = f2(-m_use, -m_use);
+        uint64_t sum2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};  // two chains of pair sums
         uint32_t pk[BKV / 2];
 #pragma unroll
         for (int e = 0; e < BKV; e += 2) {
-          const float p0 = fast_exp2(fmaf(v[e], a.scale_log2, -m_use));
-          const float p1 = fast_exp2(fmaf(v[e + 1], a.scale_log2, -m_use));
-          rs += p0 + p1;
+          float t0, t1;
+          f2_split(f2_fma(f2(v[e], v[e + 1]), scale2, shift2), t0, t1);
+          const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+          sum2[(e >> 1) & 1] = f2_add(sum2[(e >> 1) & 1], f2(p0, p1));
           pk[e / 2] = pack_bf16x2(p0, p1);
         }
-        l_run += rs;
+        float s0, s1;
+        f2_split(f2_add(sum2[0], sum2[1]), s0, s1);
+        l_run += s0 + s1;
         // P (bf16 pairs) over the first 32 columns of the scores just read.
         tmem_st_32x32b_x32(tmem + lane_base + C::s_col(x, buf), pk);
         if (any_pv && __any_sync(0xffffffffu, raise)) {
