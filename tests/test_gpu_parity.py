@@ -106,6 +106,9 @@ SWA_CASES = [  # batch, heads, seq, head_dim, window
     (1, 1, 1, 64, 1), (1, 2, 63, 64, 5), (2, 3, 64, 64, 64), (1, 2, 65, 32, 64),
     (2, 2, 200, 128, 17), (1, 4, 333, 96, 100), (1, 2, 257, 16, 1), (1, 2, 300, 64, 300),
     (1, 1, 500, 128, 2000), (2, 2, 1000, 128, 129), (1, 2, 700, 96, 511), (1, 1, 130, 32, 2),
+    # Several items per CTA (256 items), up to 20 key tiles per query tile:
+    # exercises the stage and score-buffer barrier phases across items.
+    (2, 16, 2048, 96, 1000),
 ]
 
 
