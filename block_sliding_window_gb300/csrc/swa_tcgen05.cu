@@ -390,9 +390,17 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
         // three-input max per two scores, one f32x2 FMA (scale, shift) and
         // one f32x2 add (row sum) per pair; the softmax warps are bound by
         // instruction issue, not by the exponent unit.
-        float mx = -INFINITY;
+        // Row max as a tree of depth 4 (64 -> 22 -> 8 -> 3 -> 1) rather than
+        // a chain: only two softmax warps share an SMSP to hide latency.
+        static_assert(BKV == 64, "max tree sized for 64 scores");
+        float m1[22], m2[8];
 #pragma unroll
-        for (int e = 0; e < BKV; e += 2) mx = fmax3(mx, v[e], v[e + 1]);
+        for (int t = 0; t < 21; ++t) m1[t] = fmax3(v[3 * t], v[3 * t + 1], v[3 * t + 2]);
+        m1[21] = v[63];
+#pragma unroll
+        for (int t = 0; t < 7; ++t) m2[t] = fmax3(m1[3 * t], m1[3 * t + 1], m1[3 * t + 2]);
+        m2[7] = m1[21];
+        float mx = fmax3(fmax3(m2[0], m2[1], m2[2]), fmax3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
         mx *= a.scale_log2;  // row max in the log2 domain
         // Raise the reference max only when the row max passes it by 2^8.
         float alpha = 1.f;
@@ -404,18 +412,18 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
         }
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
         const uint64_t scale2 = f2(a.scale_log2, a.scale_log2), shift2 = f2(-m_use, -m_use);
-        uint64_t sum2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};  // two chains of pair sums
+        uint64_t sum2[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
         uint32_t pk[BKV / 2];
 #pragma unroll
         for (int e = 0; e < BKV; e += 2) {
           float t0, t1;
           f2_split(f2_fma(f2(v[e], v[e + 1]), scale2, shift2), t0, t1);
           const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
-          sum2[(e >> 1) & 1] = f2_add(sum2[(e >> 1) & 1], f2(p0, p1));
+          sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2(p0, p1));  // four chains
           pk[e / 2] = pack_bf16x2(p0, p1);
         }
         float s0, s1;
-        f2_split(f2_add(sum2[0], sum2[1]), s0, s1);
+        f2_split(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), s0, s1);
         l_run += s0 + s1;
         // P (bf16 pairs) over the first 32 columns of the scores just read.
         tmem_st_32x32b_x32(tmem + lane_base + C::s_col(x, buf), pk);
