@@ -163,8 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
   uint64_t* mv_empty = mv_full + NS;    // [NS]
   uint64_t* s_full = mv_empty + NS;     // [2]
   uint64_t* p_full = s_full + 2;        // [2]
-  uint64_t* acc_done = p_full + 2;      // [2]: accumulate MMAs of buffer 0 / 1 done
-  uint64_t* acc_full = acc_done + 2;
+  uint64_t* acc_full = p_full + 2;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* done_bar = acc_empty + 1;   // [3]: one per issuing thread
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 3);
@@ -183,7 +182,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
     for (int k = 0; k < 2; ++k) {
       mbar_init(&s_full[k], 2);  // S and dP of one buffer, from two threads
       mbar_init(&p_full[k], 8);
-      mbar_init(&acc_done[k], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 8);
@@ -293,9 +291,13 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
             // Scores of the stationary rows against the moving tile:
             //   kKV: S^T = K Q^T, dP^T = V dO^T;  kQ: S = Q K^T, dP = dO V^T.
             // Buffer n % 2 holds P / dS of tile n - 2 until its accumulate
-            // MMAs have finished.
+            // MMAs have finished, which is when the accumulate thread's
+            // commit releases tile n - 2's moving stage.  (Every tile is
+            // processed, so n is also the moving-tile number.)  That phase is
+            // exact: the stage's next release needs score tile n - 2 + NS.
             if (n >= 2) {
-              if (!mbar_wait(&acc_done[n & 1], ((n - 2) >> 1) & 1, abort_flag, a.status)) {
+              const uint32_t m2 = n - 2;
+              if (!mbar_wait(&mv_empty[m2 % NS], (m2 / NS) & 1, abort_flag, a.status)) {
                 ok = false;
                 break;
               }
@@ -352,7 +354,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
                              sw128_mnmajor_desc(mv0 + kk * 16 * 128, BC * 128), idesc_acc,
                              (!first || kk > 0) ? 1u : 0u);
             }
-            umma_commit(&acc_done[n & 1]);
             umma_commit(&mv_empty[st]);
           }
           ++issued;
