@@ -8,9 +8,10 @@
 //   dgamma = sum over rows of dxn * xh,   dbeta = sum over rows of dxn.
 // Three launches, all deterministic:
 //   ln_bwd_rows_kernel     one CTA per row: dx (two block reductions).
-//   ln_bwd_columns_kernel  one thread per column and chunk of 32 rows:
+//   ln_bwd_columns_kernel  one thread per column pair and chunk of 32 rows:
 //                          partial sums of dxn * xh and dxn in row order.
-//   ln_bwd_reduce_kernel   one thread per column: the chunk partials in order.
+//   ln_bwd_reduce_kernel   one lane per column, 8 warps over the chunks: the
+//                          chunk partials summed in a fixed order.
 #include "ptb_device.cuh"
 
 namespace ptb {
@@ -90,40 +91,62 @@ __global__ void __launch_bounds__(kThreads) ln_bwd_rows_kernel(
 }
 
 // partials[chunk][0][c] = sum over the chunk's rows of dxn * xh,
-// partials[chunk][1][c] = sum of dxn, rows in increasing order.
+// partials[chunk][1][c] = sum of dxn, rows in increasing order.  A thread
+// takes two adjacent columns (bf16x2 / float2 loads; hidden is a multiple of
+// 8), and the rows are unrolled by 8 so that 16 loads are in flight.
 __global__ void ln_bwd_columns_kernel(const __nv_bfloat16* __restrict__ x,
                                       const float2* __restrict__ stats,
                                       const float* __restrict__ dxn, int64_t rows, int hidden,
                                       float* __restrict__ partials) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  const int c = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
   if (c >= hidden) return;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kChunkRows;
   const int64_t r1 = r0 + kChunkRows < rows ? r0 + kChunkRows : rows;
-  float sgx = 0.f, sd = 0.f;
+  float sgx0 = 0.f, sgx1 = 0.f, sd0 = 0.f, sd1 = 0.f;
 #pragma unroll 8
   for (int64_t r = r0; r < r1; ++r) {
     const float2 st = __ldg(stats + r);
-    const float d = __ldg(dxn + r * hidden + c);
-    const float xh = (__bfloat162float(x[r * hidden + c]) - st.x) * st.y;
-    sgx += d * xh;
-    sd += d;
+    const float2 d = __ldg(reinterpret_cast<const float2*>(dxn + r * hidden + c));
+    const uint32_t xv = __ldg(reinterpret_cast<const unsigned int*>(x + r * hidden + c));
+    sgx0 += d.x * ((bf16_lo(xv) - st.x) * st.y);
+    sgx1 += d.y * ((bf16_hi(xv) - st.x) * st.y);
+    sd0 += d.x;
+    sd1 += d.y;
   }
-  partials[(static_cast<int64_t>(blockIdx.y) * 2) * hidden + c] = sgx;
-  partials[(static_cast<int64_t>(blockIdx.y) * 2 + 1) * hidden + c] = sd;
+  const int64_t base = static_cast<int64_t>(blockIdx.y) * 2 * hidden + c;
+  *reinterpret_cast<float2*>(partials + base) = make_float2(sgx0, sgx1);
+  *reinterpret_cast<float2*>(partials + base + hidden) = make_float2(sd0, sd1);
 }
 
-__global__ void ln_bwd_reduce_kernel(const float* __restrict__ partials, int64_t chunks,
-                                     int hidden, float* __restrict__ dgamma,
-                                     float* __restrict__ dbeta) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= hidden) return;
+// dgamma / dbeta: the chunk partials of a column summed in a fixed order.
+// A CTA takes 32 columns (lane = column); its 8 warps each sum every 8th
+// chunk in increasing order, and warp 0 adds the 8 warp sums in warp order.
+__global__ void __launch_bounds__(kThreads) ln_bwd_reduce_kernel(
+    const float* __restrict__ partials, int64_t chunks, int hidden, float* __restrict__ dgamma,
+    float* __restrict__ dbeta) {
+  __shared__ float red[2][kThreads / 32][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + lane;
   float a = 0.f, b = 0.f;
-  for (int64_t k = 0; k < chunks; ++k) {
-    a += partials[(2 * k) * hidden + c];
-    b += partials[(2 * k + 1) * hidden + c];
+  if (c < hidden) {
+    for (int64_t k = warp; k < chunks; k += kThreads / 32) {
+      a += __ldg(partials + (2 * k) * hidden + c);
+      b += __ldg(partials + (2 * k + 1) * hidden + c);
+    }
   }
-  dgamma[c] = a;
-  dbeta[c] = b;
+  red[0][warp][lane] = a;
+  red[1][warp][lane] = b;
+  __syncthreads();
+  if (warp == 0 && c < hidden) {
+    float ta = 0.f, tb = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      ta += red[0][w][lane];
+      tb += red[1][w][lane];
+    }
+    dgamma[c] = ta;
+    dbeta[c] = tb;
+  }
 }
 
 }  // namespace
@@ -143,12 +166,12 @@ cudaError_t launch_layernorm_backward(const __nv_bfloat16* x, const __nv_bfloat1
                                                                           dy, hidden, dx);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const dim3 grid((hidden + kThreads - 1) / kThreads, static_cast<unsigned>(chunks));
+  const dim3 grid((hidden / 2 + kThreads - 1) / kThreads, static_cast<unsigned>(chunks));
   ln_bwd_columns_kernel<<<grid, kThreads, 0, stream>>>(x, stats, dxn, rows, hidden, partials);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  ln_bwd_reduce_kernel<<<(hidden + kThreads - 1) / kThreads, kThreads, 0, stream>>>(
-      partials, chunks, hidden, dgamma, dbeta);
+  ln_bwd_reduce_kernel<<<(hidden + 31) / 32, kThreads, 0, stream>>>(partials, chunks, hidden,
+                                                                   dgamma, dbeta);
   return cudaGetLastError();
 }
 
