@@ -387,16 +387,28 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
         nlse_row = -a.lse[bh * a.seq + row];
         delta_row = a.delta[bh * a.seq + row];
       }
+      // kKV: lane j carries -lse and delta of query column j of the tile
+      // (negated lse: one FMA below).  They are loaded one tile ahead, so
+      // the global-load latency (~800 cycles measured) overlaps a tile's
+      // work instead of stalling each tile's start.
+      auto col_stats = [&](int t, float& nl, float& dl) {
+        const int q = (it.t_lo + t) * BC + grp * kGroupCols + lane;
+        const bool in = t < it.n_tiles && q < a.seq;
+        nl = in ? -__ldg(a.lse + bh * a.seq + q) : 0.f;
+        dl = in ? __ldg(a.delta + bh * a.seq + q) : 0.f;
+      };
+      float nl_next = 0.f, dl_next = 0.f;
+      if (MODE == kKV) col_stats(0, nl_next, dl_next);
       for (int t = 0; t < it.n_tiles; ++t) {
         // First moving position of this warpgroup's 32 columns of the tile.
         const int c0 = (it.t_lo + t) * BC + grp * kGroupCols;
         const int buf = seen & 1;
-        if (MODE == kKV) {  // per-query lse and delta of the columns, staged per warp
+        if (MODE == kKV) {  // staged per warp for broadcast reads
           __syncwarp();
-          const int q = c0 + lane;
-          wl[lane] = q < a.seq ? -a.lse[bh * a.seq + q] : 0.f;  // negated: one FMA below
-          wl[kGroupCols + lane] = q < a.seq ? a.delta[bh * a.seq + q] : 0.f;
+          wl[lane] = nl_next;
+          wl[kGroupCols + lane] = dl_next;
           __syncwarp();
+          col_stats(t + 1, nl_next, dl_next);
         }
         if (!mbar_wait_warp(&s_full[buf], (seen >> 1) & 1, abort_flag, a.status)) {
           ok = false;
