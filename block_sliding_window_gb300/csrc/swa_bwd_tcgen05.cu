@@ -391,11 +391,17 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
       // (negated lse: one FMA below).  They are loaded one tile ahead, so
       // the global-load latency (~800 cycles measured) overlaps a tile's
       // work instead of stalling each tile's start.
+      // (The loads are volatile asm, so the compiler keeps them here, ahead
+      // of the tile's barrier wait, rather than next to their use.)
       auto col_stats = [&](int t, float& nl, float& dl) {
         const int q = (it.t_lo + t) * BC + grp * kGroupCols + lane;
         const bool in = t < it.n_tiles && q < a.seq;
-        nl = in ? -__ldg(a.lse + bh * a.seq + q) : 0.f;
-        dl = in ? __ldg(a.delta + bh * a.seq + q) : 0.f;
+        const int64_t off = in ? bh * a.seq + q : 0;  // row 0 always exists
+        float l, d;
+        asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(l) : "l"(a.lse + off));
+        asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(d) : "l"(a.delta + off));
+        nl = in ? -l : 0.f;
+        dl = in ? d : 0.f;
       };
       float nl_next = 0.f, dl_next = 0.f;
       if (MODE == kKV) col_stats(0, nl_next, dl_next);
