@@ -114,27 +114,6 @@ __device__ __forceinline__ Item decode_item(const BwdParams& P, int item) {
   return it;
 }
 
-// D columns of one TMEM lane row (fp32) into v.
-template <int D>
-__device__ __forceinline__ void tmem_row(uint32_t taddr, float (&v)[D]) {
-  if constexpr (D % 32 == 0) {
-#pragma unroll
-    for (int c = 0; c < D; c += 32) {
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(taddr + c, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 32; ++e) v[c + e] = __uint_as_float(r[e]);
-    }
-  } else {
-    uint32_t r[16];
-    tmem_ld_32x32b_x16(taddr, r);
-    tmem_ld_wait();
-#pragma unroll
-    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
-  }
-}
-
 template <int D>
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float (&v)[D], float mul) {
 #pragma unroll
@@ -498,24 +477,47 @@ __global__ void __launch_bounds__(kThreads, 1) swa_bwd_kernel(const __grid_const
       }
       tc_fence_after();
       const int prow = row < a.seq ? row : 0;
-      float g[D];
-      if constexpr (MODE == kKV) {  // warpgroup 0: dV, warpgroup 1: dK
-        tmem_row<D>(tmem + lane_base + C::acc_col(grp), g);
-        if (row < a.seq) {
-          if (grp == 0)
-            store_row_bf16<D>(a.dv + it.b * a.dv_sb + it.h * a.dv_sh + prow * a.dv_ss, g, 1.f);
-          else
-            store_row_bf16<D>(a.dk + it.b * a.dk_sb + it.h * a.dk_sh + prow * a.dk_ss, g,
-                              a.scale);
+      // kKV: warpgroup 0 stores dV, warpgroup 1 dK; kQ: warpgroup 0 dQ.
+      // Up to 64 columns are loaded per wait, and a warp releases the
+      // accumulators right after its last TMEM load has landed: the next
+      // item's accumulate MMAs do not wait for the stores.
+      const bool active = MODE == kKV || grp == 0;
+      __nv_bfloat16* dst =
+          MODE == kQ ? a.dq + it.b * a.dq_sb + it.h * a.dq_sh + prow * a.dq_ss
+          : grp == 0 ? a.dv + it.b * a.dv_sb + it.h * a.dv_sh + prow * a.dv_ss
+                     : a.dk + it.b * a.dk_sb + it.h * a.dk_sh + prow * a.dk_ss;
+      const float mul = MODE == kKV && grp == 0 ? 1.f : a.scale;
+      const uint32_t tacc = tmem + lane_base + C::acc_col(active ? grp : 0);
+      constexpr int kGrp = D % 64 == 0 ? 64 : D % 32 == 0 ? 32 : D;  // columns per wait
+      static_assert(D % kGrp == 0 && kGrp % 8 == 0, "whole groups of whole 16-byte stores");
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += kGrp) {
+        float g[kGrp];
+        if (active) {
+          if constexpr (kGrp % 32 == 0) {
+            uint32_t r[kGrp / 32][32];
+#pragma unroll
+            for (int h = 0; h < kGrp / 32; ++h) tmem_ld_32x32b_x32(tacc + c0 + 32 * h, r[h]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < kGrp / 32; ++h)
+#pragma unroll
+              for (int e = 0; e < 32; ++e) g[32 * h + e] = __uint_as_float(r[h][e]);
+          } else {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(tacc + c0, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) g[e] = __uint_as_float(r[e]);
+          }
         }
-      } else if (grp == 0) {
-        tmem_row<D>(tmem + lane_base + C::acc_col(0), g);
-        if (row < a.seq)
-          store_row_bf16<D>(a.dq + it.b * a.dq_sb + it.h * a.dq_sh + prow * a.dq_ss, g, a.scale);
+        if (c0 + kGrp >= D) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty);
+        }
+        if (active && row < a.seq) store_row_bf16<kGrp>(dst + c0, g, mul);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
       ++items_done;
     }
   }
