@@ -212,9 +212,11 @@ ptb_status gemm_run(DeviceState* ds, const GemmSpec& g, int64_t tokens, ptb_bf16
   a.k_split = static_cast<int>(g.k1 ? g.k0 : K);
   a.layout = kLayoutKK;
   a.n_fastest = 0;
-  // The first GEMM re-reads xn for every N tile; the weights and the second
-  // GEMM's A are streamed.
-  a.a_keep = resid ? 0 : 1;
+  // A is re-read by every wave of N tiles (xn in the first GEMM, [ctx | G]
+  // in the second), so it is kept in L2 ahead of the weights, which each
+  // wave streams once.  (Keeping the second GEMM's A: 530B-class layer 2.5%
+  // faster, 175B-class 0.3%, 13B-class unchanged.)
+  a.a_keep = 1;
   a.b_keep = 0;
   a.out = bf(out);
   a.ld_out = ldo;
