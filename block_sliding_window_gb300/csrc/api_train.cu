@@ -67,6 +67,9 @@ GemmCall call_dgrad_in(int64_t t, int64_t h, int64_t f, int64_t ldu) {  // dU1 [
   c.epilogue = kEpiF32;
   c.M = t, c.N = h, c.K = ldu, c.k_split = 3 * h;
   c.lda0 = ldu, c.lda1 = ldu, c.ldb0 = h, c.ldb1 = h;
+  // dU1 is re-read by every wave of N tiles, the weights once: keep dU1 in
+  // L2 (175B-class: this GEMM 2.75 -> 2.70 ms).
+  c.a_keep = true;
   (void)f;
   return c;
 }
