@@ -567,7 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 // TMEM receives its 128 rows of the accumulator.  Per SM and 64-wide k-block
 // the stage is 32 KB instead of 48 KB, so the shared-memory traffic of TMA
 // writes plus operand reads drops by a third.
-//   warp 0      both ranks: TMA producer into their own 6-stage ring.  The
+//   warp 0      both ranks: TMA producer into their own ring of 5 or 6
+//               stages (pair_stages).  The
 //               copies of both ranks complete on rank 0's `full` barrier of
 //               the stage (cta_group::2 TMA), which rank 0 arms with the
 //               bytes of both.  (A first version relayed rank 1's stages with
@@ -581,8 +582,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 // The remainder wave is split along K per pair as in the single-CTA kernel
 // (256-row partial tiles, 8 arrival counters per tile).
 constexpr int kPairBN = 256;
-constexpr int kPairStages = 6;
-template <bool STAGE = false>
+// Stages of the ring.  Fewer stages leave more of the SM's unified L1 /
+// shared memory to L1.  Measured at the 13B-class shapes: the
+// [out | down] and input-gradient GEMMs are 2.5-4.4% faster with 5 stages
+// than with 6, the [QKV | up] GEMM 1.7% slower; 7 stages (231 KB) were
+// 10-15% slower.
+template <int EPI>
+__host__ __device__ constexpr int pair_stages() { return EPI == kEpiQkvGelu ? 6 : 5; }
+template <bool STAGE = false, int NSTAGES = 6>
 struct PairCfg {
   static constexpr int kABytes = BM * 128;
   static constexpr int kBBytes = (kPairBN / 2) * 128;
@@ -590,18 +597,18 @@ struct PairCfg {
   static constexpr int kTmemCols = 2 * kPairBN;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemBytes =
-      kPairStages * kStageBytes + kBarBytes + (STAGE ? kF32StageBytes : 0) + 1024;
+      NSTAGES * kStageBytes + kBarBytes + (STAGE ? kF32StageBytes : 0) + 1024;
 };
 
 template <int EPI, int LAYOUT, bool FP8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ GemmArgs p) {
   constexpr bool kStage = staged_f32<EPI, LAYOUT>();
-  using C = PairCfg<kStage>;
+  using C = PairCfg<kStage, pair_stages<EPI>()>;
   constexpr int BN = kPairBN;
   constexpr int BK = Elem<FP8>::kBK;
   static_assert(!(FP8 && LAYOUT != kLayoutKK), "e4m3 operands are K-major only");
-  constexpr int NS = kPairStages;
+  constexpr int NS = pair_stages<EPI>();
   // MN-major operands arrive as 64-wide MN blocks of 64 K rows (8 KB each).
   constexpr bool kAmn = (LAYOUT & 1) != 0;
   constexpr bool kBmn = (LAYOUT & 2) != 0;
@@ -820,7 +827,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 template <int EPI, int LAYOUT, bool FP8 = false>
 cudaError_t launch_pair(const GemmArgs& a, cudaStream_t stream) {
-  using C = PairCfg<staged_f32<EPI, LAYOUT>()>;
+  using C = PairCfg<staged_f32<EPI, LAYOUT>(), pair_stages<EPI>()>;
   auto kern = gemm_pair_kernel<EPI, LAYOUT, FP8>;
   static int configured_device = -1;
   int dev = 0;
