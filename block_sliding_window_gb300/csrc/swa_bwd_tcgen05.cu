@@ -630,6 +630,9 @@ cudaError_t launch_swa_backward(const SwaBwdArgs& a, cudaStream_t stream) {
   }
   BwdParams prm;
   prm.a = a;
+  // A window of s or more is plain causal attention; clamping it keeps every
+  // index expression of the kernels (a row plus the window, ...) inside int.
+  if (prm.a.window > prm.a.seq) prm.a.window = prm.a.seq;
   prm.blocks = (a.seq + BR - 1) / BR;
   const int64_t items = static_cast<int64_t>(prm.blocks) * a.heads * a.batch;
   if (items > 0x3fffffff) return cudaErrorInvalidValue;  // item numbers stay in int

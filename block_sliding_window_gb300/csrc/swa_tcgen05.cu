@@ -570,6 +570,9 @@ cudaError_t launch_swa(const SwaArgs& a, cudaStream_t stream) {
   if (a.seq <= 0 || a.batch <= 0 || a.heads <= 0) return cudaSuccess;
   SwaParams prm;
   prm.a = a;
+  // A window of s or more is plain causal attention; clamping it keeps every
+  // index expression of the kernels (a row plus the window, ...) inside int.
+  if (prm.a.window > prm.a.seq) prm.a.window = prm.a.seq;
   int sd_q = 0, sd_k = 0, sd_v = 0;
   // With one batch entry the batch stride is never used; a non-positive one
   // is replaced by a harmless positive value for the tensor map.

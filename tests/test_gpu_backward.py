@@ -103,6 +103,19 @@ def test_swa_backward_operator(ptb_lib, b, h, s, d, w):
         assert_grad_close(got, ref, f"SWA b{b}h{h}s{s}d{d}w{w} {name}")
 
 
+def test_swa_backward_window_at_int32_max(ptb_lib):
+    """Any window >= s is plain causal attention: the backward pass with
+    w = 2^31 - 1 gives the same bits as with w = s."""
+    b, h, s, d = 1, 2, 300, 128
+    q, k, v = (t.cuda() for t in workloads.swa_inputs(b, h, s, d, seed=32))
+    dout = workloads.normal_bf16((b, h, s, d), seed=33).cuda()
+    o, lse = ptb_lib.swa_attention_lse(q, k, v, s)
+    got_big = ptb_lib.swa_attention_backward(q, k, v, o, dout, lse, 2**31 - 1)
+    got_s = ptb_lib.swa_attention_backward(q, k, v, o, dout, lse, s)
+    for name, g_big, g_s in zip(("dq", "dk", "dv"), got_big, got_s):
+        assert torch.equal(g_big, g_s), name
+
+
 def test_swa_backward_unit_window(ptb_lib):
     """w = 1: P is the identity, so dv = dout bit for bit and dq = dk = 0 up
     to the rounding residue described at ZERO_TOL."""

@@ -154,6 +154,19 @@ def test_swa_operator_config(ptb_lib, w):
     assert np.array_equal(counts.cpu().numpy(), want_counts)
 
 
+def test_swa_window_at_int32_max(ptb_lib):
+    """Any window >= s is plain causal attention: w = 2^31 - 1 gives the same
+    bits as w = s (no index arithmetic may overflow on the way)."""
+    b, h, s, d = 1, 2, 300, 96
+    q, k, v = (t.cuda() for t in workloads.swa_inputs(b, h, s, d, seed=31))
+    o_big, counts = ptb_lib.swa_attention_counts(q, k, v, 2**31 - 1)
+    o_s = ptb_lib.swa_attention(q, k, v, s)
+    assert torch.equal(o_big, o_s)
+    assert np.array_equal(counts.cpu().numpy(),
+                          np.broadcast_to(oracle.attended_counts(s, s), (b, h, s)))
+    assert_close(o_big, oracle.swa(q.cpu(), k.cpu(), v.cpu(), s), "SWA w = 2^31 - 1")
+
+
 def test_swa_strided_in_place(ptb_lib):
     """Q, K, V as head-strided column blocks of one [T, 3H + F] buffer and the
     output written over Q, as the layer does."""
