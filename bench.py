@@ -54,6 +54,13 @@ def layer_flops(cfg) -> dict:
             "band_keys": band * cfg.batch * cfg.heads}
 
 
+def swa_flops(cfg) -> int:
+    """Algorithmic FLOPs of the SWA operator: Q K^T and P V over the in-band
+    (query, key) pairs only, 4 d per pair and head."""
+    band = sum(min(i + 1, cfg.window) for i in range(cfg.seq))
+    return 4 * cfg.batch * cfg.heads * cfg.head_dim * band
+
+
 def backward_flops(cfg) -> dict:
     """Algorithmic backward FLOPs: an input-gradient and a weight-gradient
     GEMM per forward GEMM, and dV, dP, dQ, dK over the in-band pairs."""
@@ -302,7 +309,7 @@ def run_swa(args, world, rank, local):
     ms = max_over_ranks(kern_ms, world)
     band = sum(min(i + 1, cfg.window) for i in range(cfg.seq))
     tokens = cfg.batch * cfg.seq
-    flops = 4 * cfg.batch * cfg.heads * cfg.head_dim * band
+    flops = swa_flops(cfg)
     bytes_ = 4 * q.numel() * 2
     peaks, peak_src = load_peaks()
     ach = bytes_ / (kern_ms * 1e-3) / 1e9
@@ -432,8 +439,10 @@ def run_train(args, world, rank, local):
                     "median": statistics.median(per_step), "min": min(per_step)},
         "flops": {"forward": fwd["total"], "backward": bwd["total"]},
         "roofline": {"bound": "tensor", "kernel": f"{top} (tcgen05 GEMM, backward)",
-                     "achieved": top_tf, "peak": peak_sus, "unit": "TFLOP/s",
-                     "frac": top_tf / peak_sus, "peak_source": f"{peak_src} bf16 sustained",
+                     "achieved": top_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": top_tf / peaks["bf16_tflops"],
+                     "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "frac_of_sustained": top_tf / peak_sus,
                      "traffic": traffic_for(top, args.workload + "_train", GEMM_SRC),
                      "algorithmic_flops_per_launch": bwd[top]},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
@@ -592,15 +601,22 @@ def run_ours(args, world, rank, local):
     roofline = None
     if per_kernel:
         g1_tf = fl["gemm1"] / (per_kernel["gemm_qkv_up"] * 1e-3) / 1e12
+        # The timed region is a fraction of a second, so the denominator is
+        # the burst (dense) peak; the fraction of the seconds-long sustained
+        # figure is reported beside it, labelled.
         roofline = {"bound": "tensor", "kernel": "gemm_qkv_up (tcgen05 [QKV|up] GEMM + GELU)",
-                    "achieved": g1_tf, "peak": peak_sus, "unit": "TFLOP/s",
-                    "frac": g1_tf / peak_sus, "peak_source": f"{peak_src} bf16 sustained",
+                    "achieved": g1_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": g1_tf / peaks["bf16_tflops"],
+                    "peak_source": f"{peak_src} bf16 dense (burst)",
+                    "frac_of_sustained": g1_tf / peak_sus,
                     "traffic": traffic_for("gemm_qkv_up", args.workload, GEMM_SRC),
                     "algorithmic_flops_per_launch": fl["gemm1"]}
-        if fp8:  # e4m3 peak = measured bf16 sustained x the nominal 4.5 : 2.25 ratio
+        if fp8:  # e4m3 peak = measured bf16 x the nominal 4.5 : 2.25 dense ratio
+            fp8_burst = 2.0 * peaks["bf16_tflops"]
             roofline.update(kernel="gemm_qkv_up (tcgen05 e4m3 [QKV|up] GEMM + GELU)",
-                            peak=2.0 * peak_sus, frac=g1_tf / (2.0 * peak_sus),
-                            peak_source=f"{peak_src} bf16 sustained x 2 (nominal e4m3:bf16)",
+                            peak=fp8_burst, frac=g1_tf / fp8_burst,
+                            peak_source=f"{peak_src} bf16 dense (burst) x 2 (nominal e4m3:bf16)",
+                            frac_of_sustained=g1_tf / (2.0 * peak_sus),
                             traffic=traffic_for("fp8_gemm_qkv_up", args.workload, GEMM_SRC))
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -623,10 +639,12 @@ def run_ours(args, world, rank, local):
     if fp8:
         line["dtype"] = "e4m3 GEMM operands (per-row scales), bf16 activations and attention"
         line["gpu_launches"] = 5 * args.steps
-        fp8_peak = 2.0 * peak_sus  # nominal e4m3 / bf16 dense ratio 4.5 / 2.25
-        line["pct_of_peak"] = {"fp8_sustained_nominal_ratio": 100 * tflops / world / fp8_peak,
-                               "bf16_burst": 100 * tflops / world / peaks["bf16_tflops"],
-                               "source": f"{peak_src} bf16 x 2"}
+        # nominal e4m3 / bf16 dense ratio 4.5 / 2.25
+        line["pct_of_peak"] = {
+            "fp8_burst_nominal_ratio": 100 * tflops / world / (2.0 * peaks["bf16_tflops"]),
+            "fp8_sustained_nominal_ratio": 100 * tflops / world / (2.0 * peak_sus),
+            "bf16_burst": 100 * tflops / world / peaks["bf16_tflops"],
+            "source": f"{peak_src} bf16 x 2"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not serial and not fp8:
         f64 = oracle_sample(cfg, args.cpu_rows, seed_device="cuda")
         times = time_oracle(cfg, f64, args.cpu_rows, 1)

@@ -71,7 +71,7 @@ SYMBOLS = {
     "ptb_gemm_qkv_up": (_st, [_p, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]),
     "ptb_gemm_out_down": (_st, [_p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p, _p, _sz,
                                 _p]),
-    "ptb_last_device_error": (_st, []),
+    "ptb_last_device_error": (_st, [_p]),
     "ptb_wait_probe": (_st, [ctypes.c_uint64, _p]),
 }
 
@@ -530,9 +530,10 @@ def release_workspace() -> None:
     _check(load().ptb_release_workspace(), "ptb_release_workspace")
 
 
-def last_device_error() -> int:
-    """Synchronises and returns (and clears) the kernels' device status word."""
-    return int(load().ptb_last_device_error())
+def last_device_error(stream=None) -> int:
+    """Waits for `stream` (default: the current stream) and returns (and
+    clears) the kernels' device status word."""
+    return int(load().ptb_last_device_error(_stream(stream)))
 
 
 def wait_probe(limit_ns: int, stream=None) -> None:

@@ -31,6 +31,8 @@ struct DeviceState {
   // apply (environment variable PTB_GEMM_PAIRS=0 / 1 overrides the default).
   int pairs = -1;
   unsigned* status = nullptr;
+  // Device word that ptb_last_device_error swaps the status word into.
+  unsigned* status_taken = nullptr;
   void* arena = nullptr;
   size_t arena_bytes = 0;
 };

@@ -22,9 +22,14 @@ namespace api {
 constexpr int kMaxDevices = 64;
 
 __device__ unsigned g_status_word;
+// Where take_status_kernel leaves the word it swapped out, for the host to read.
+__device__ unsigned g_status_taken;
 
 
 std::mutex g_mutex;
+// Serialises ptb_last_device_error calls: they share the device word that
+// the status is swapped into.
+std::mutex g_status_mutex;
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -47,6 +52,8 @@ ptb_status device_state(DeviceState** out) {
     void* sym = nullptr;
     if (cudaGetSymbolAddress(&sym, g_status_word) != cudaSuccess) return PTB_ERR_DEVICE;
     s.status = static_cast<unsigned*>(sym);
+    if (cudaGetSymbolAddress(&sym, g_status_taken) != cudaSuccess) return PTB_ERR_DEVICE;
+    s.status_taken = static_cast<unsigned*>(sym);
     if (!g_encode) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -416,6 +423,13 @@ __global__ void wait_probe_kernel(uint64_t limit_ns, unsigned* status) {
   }
 }
 
+// Reads and clears the status word in one atomic step, so that a code
+// recorded by a kernel on another stream between a read and a clear is
+// never lost.
+__global__ void take_status_kernel(unsigned* status, unsigned* taken) {
+  *taken = atomicExch(status, 0u);
+}
+
 }  // namespace api
 
 bool make_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
@@ -783,16 +797,18 @@ ptb_status ptb_gemm_out_down(const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16
                        workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
-ptb_status ptb_last_device_error(void) {
+ptb_status ptb_last_device_error(ptb_stream stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   DeviceState* ds = nullptr;
   ptb_status st = device_state(&ds);
   if (st != PTB_OK) return st;
-  if (cudaDeviceSynchronize() != cudaSuccess) return PTB_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lock(g_status_mutex);
+  take_status_kernel<<<1, 1, 0, stream>>>(ds->status, ds->status_taken);
+  if (cudaGetLastError() != cudaSuccess) return PTB_ERR_LAUNCH;
   unsigned word = 0;
-  if (cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return PTB_ERR_LAUNCH;
-  const unsigned zero = 0;
-  if (cudaMemcpy(ds->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+  if (cudaMemcpyAsync(&word, ds->status_taken, sizeof(word), cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
     return PTB_ERR_LAUNCH;
   return static_cast<ptb_status>(word);
 }

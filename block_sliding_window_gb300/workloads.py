@@ -117,12 +117,18 @@ def normal_bf16(shape, seed: int, std: float = 1.0, mean: float = 0.0,
     return (t * std + mean).to(torch.bfloat16)
 
 
-def sample_rows(seq: int, window: int) -> list:
-    """Sequence positions checked one by one on the full-size layers: the
-    first rows, the tile edges around 64 and 128, the window edge and the
-    last rows."""
+def sample_rows(seq: int, window: int, tile: int = 128) -> list:
+    """Sequence positions checked one by one on the full-size layers.
+
+    The first rows, the edges around 64 and 128, the window edge and the last
+    rows, plus one row inside every `tile`-row block of the sequence (the
+    GEMMs' M tiles and the attention's query tiles are 128 rows).  The row
+    inside block t sits at offset (37 t + 17) mod tile, so successive blocks
+    probe different 32-row quarters (different TMEM lane groups)."""
     cand = {0, 1, 2, 63, 64, 127, 128, 129, window - 1, window, window + 1,
             seq // 2, seq - 2, seq - 1}
+    for t in range((seq + tile - 1) // tile):
+        cand.add(t * tile + (37 * t + 17) % tile)
     return sorted(r for r in cand if 0 <= r < seq)
 
 

@@ -25,13 +25,14 @@
  *     as raw 16-bit patterns (ptb_bf16).
  *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL
  *     is the legacy default stream) on the current CUDA device.  No entry
- *     point synchronises except ptb_last_device_error().
+ *     point synchronises except ptb_last_device_error(stream), which waits
+ *     for that one stream.
  *   - Argument errors are detected on the host before anything is launched
  *     and returned as a ptb_status; nothing is written in that case.
  *   - Kernels never trap.  A device-side wait that does not complete within
  *     about two seconds makes the kernel give up, record PTB_ERR_TIMEOUT in
- *     the per-device status word and return; ptb_last_device_error() reads
- *     and clears that word.
+ *     the per-device status word and return; ptb_last_device_error(stream)
+ *     reads and clears that word.
  */
 #ifndef PTB_H_
 #define PTB_H_
@@ -140,7 +141,6 @@ ptb_status ptb_forward_host(const ptb_bf16* x_host, const ptb_bf16* ln_gamma,
                             size_t workspace_bytes, ptb_stream stream);
 
 /*
- * ptb_forward_noalloc:/*
  * ptb_forward_noalloc: ptb_forward for callers that cannot allocate device
  * memory.  The paper has no counterpart; this is a deployment convenience.
  *
@@ -318,7 +318,7 @@ ptb_status ptb_backward_events(const ptb_bf16* dy, const ptb_bf16* x, const ptb_
  */
 ptb_status ptb_set_gemm_pairs(int32_t mode, int32_t* previous);
 
-/* Frees the library's own workspace arena/* Frees the library's own workspace arena on the current device (if any). */
+/* Frees the library's own workspace arena on the current device (if any). */
 ptb_status ptb_release_workspace(void);
 
 /*
@@ -431,11 +431,17 @@ ptb_status ptb_gemm_out_down(const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16
                              void* workspace, size_t workspace_bytes, ptb_stream stream);
 
 /*
- * Synchronises the current device, then returns and clears the device
- * status word written by the kernels (PTB_OK if no kernel gave up), or
- * PTB_ERR_LAUNCH if the CUDA context reports an error.
+ * ptb_last_device_error: waits for the work queued on `stream` so far
+ * (cudaStreamSynchronize of that stream only; other streams keep running),
+ * then returns the device status word written by the kernels and clears it
+ * in the same atomic step: PTB_OK if no kernel gave up, PTB_ERR_TIMEOUT if a
+ * bounded device-side wait expired, PTB_ERR_LAUNCH if the CUDA context
+ * reports an error.  The word is per device, so it also holds a code that a
+ * kernel on another stream recorded before the read.  NULL is the legacy
+ * default stream, which waits for every blocking stream of the device.
+ * Calls from several host threads are serialised inside the library.
  */
-ptb_status ptb_last_device_error(void);
+ptb_status ptb_last_device_error(ptb_stream stream);
 
 /*
  * Test hook: the wait limit of the kernels' bounded waits.  ptb_wait_probe

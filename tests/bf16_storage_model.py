@@ -98,23 +98,33 @@ def e4m3_codes_fp32(a):
     return q.view(torch.uint8), s.squeeze(-1)
 
 
+def _e4m3_linear(a, w, slab: int = 4096):
+    """a @ e4m3_rows(w).T, quantizing w (per row) a slab of rows at a time;
+    the scales are per row, so this equals quantizing w whole."""
+    f = lambda t: t.detach().to("cpu").double().numpy() if hasattr(t, "detach") else np.asarray(t, np.float64)  # noqa: E731
+    out = np.empty(a.shape[:-1] + (w.shape[0],))
+    for r0 in range(0, w.shape[0], slab):
+        out[..., r0:r0 + slab] = a @ e4m3_rows(f(w[r0:r0 + slab])).T
+    return out
+
+
 def ptb_forward_fp8_storage(x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, heads, window, rows):
     """The PTB with the FP8 path's rounding points: e4m3 xn, W1, [ctx | G] and
-    W2 (per-row scales), bf16 Q, K, V, P, ctx, G, y; exact arithmetic between."""
+    W2 (per-row scales), bf16 Q, K, V, P, ctx, G, y; exact arithmetic between.
+    W1 = [W_qkv ; W_up] and W2 = [W_o | W_down] are quantized a slab of rows
+    at a time, so the 530B-shaped weights never exist whole in fp64."""
     f = lambda t: t.detach().to("cpu").double().numpy() if hasattr(t, "detach") else np.asarray(t, np.float64)  # noqa: E731
     x0 = f(x[0])
     hidden = x0.shape[-1]
     d = hidden // heads
-    w1 = e4m3_rows(np.concatenate([f(w_qkv), f(w_up)], axis=0))
-    w2 = e4m3_rows(np.concatenate([f(w_o), f(w_down)], axis=1))
     kpos = oracle.needed_key_positions(rows, window)
     need = np.union1d(kpos, rows)
     xn = np.zeros_like(x0)
     xn[need] = e4m3_rows(oracle.layer_norm(x0[need], ln_gamma, ln_beta))
-    q = bf16(xn[rows] @ w1[0:hidden].T)
-    k = bf16(xn[kpos] @ w1[hidden:2 * hidden].T)
-    v = bf16(xn[kpos] @ w1[2 * hidden:3 * hidden].T)
-    g = bf16(oracle.gelu_tanh(xn[rows] @ w1[3 * hidden:].T))
+    q = bf16(_e4m3_linear(xn[rows], w_qkv[0:hidden]))
+    k = bf16(_e4m3_linear(xn[kpos], w_qkv[hidden:2 * hidden]))
+    v = bf16(_e4m3_linear(xn[kpos], w_qkv[2 * hidden:3 * hidden]))
+    g = bf16(oracle.gelu_tanh(_e4m3_linear(xn[rows], w_up)))
     ctx = np.zeros((len(rows), hidden))
     mask = oracle.band_mask(rows, kpos, window)
     for h in range(heads):
@@ -123,4 +133,9 @@ def ptb_forward_fp8_storage(x, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, head
         e = np.exp(sc - sc.max(axis=1, keepdims=True))
         ctx[:, sl] = (bf16(e) @ v[:, sl]) / e.sum(axis=1, keepdims=True)
     a8 = e4m3_rows(np.concatenate([bf16(ctx), g], axis=1))
-    return bf16(x0[rows] + a8 @ w2.T)
+    y = np.empty((len(rows), hidden))
+    slab = 2048
+    for r0 in range(0, hidden, slab):
+        w2 = e4m3_rows(np.concatenate([f(w_o[r0:r0 + slab]), f(w_down[r0:r0 + slab])], axis=1))
+        y[:, r0:r0 + slab] = a8 @ w2.T
+    return bf16(x0[rows] + y)

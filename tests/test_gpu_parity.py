@@ -9,6 +9,7 @@ configuration the benchmark times and are checked on sampled rows that the
 oracle computes one by one.
 """
 import math
+import time
 
 import numpy as np
 import pytest
@@ -43,6 +44,24 @@ def test_bounded_wait_gives_up_and_reports(ptb_lib):
     assert ptb_lib.last_device_error() == 6
     assert ptb_lib.last_device_error() == 0
     assert torch.ones(8, device="cuda").sum().item() == 8
+
+
+def test_status_read_waits_for_its_own_stream_only(ptb_lib):
+    """ptb_last_device_error(stream A) returns while a long kernel queued on
+    stream B is still running: it synchronises stream A, not the device."""
+    a, b = torch.cuda.Stream(), torch.cuda.Stream()
+    assert ptb_lib.last_device_error(stream=a) == 0  # kernel loaded, stream A idle
+    torch.cuda.synchronize()
+    with torch.cuda.stream(b):
+        torch.cuda._sleep(3_000_000_000)  # about 1.5 s at 2 GHz
+    t0 = time.perf_counter()
+    st = ptb_lib.last_device_error(stream=a)
+    waited = time.perf_counter() - t0
+    b_busy = not b.query()
+    torch.cuda.synchronize()
+    assert st == 0
+    assert b_busy, f"the status read on stream A waited for stream B ({waited:.3f} s)"
+    assert waited < 0.5, f"the status read on stream A took {waited:.3f} s"
 
 
 # --------------------------------------------------------------- LayerNorm --
@@ -365,8 +384,10 @@ def test_fp8_weight_codes_bit_exact(ptb_lib):
     assert float(s1z[3 * cfg.hidden + 5]) == 1.0
 
 
-@pytest.mark.parametrize("name", ["13b"])
+@pytest.mark.parametrize("name", ["13b", "175b", "530b"])
 def test_ptb_forward_fp8_full_size_sampled(ptb_lib, name):
+    """The FP8 layer at the shapes its throughput is reported on, launched as
+    the benchmark launches it, on rows in every 128-row tile."""
     cfg = workloads.PTB_CONFIGS[name]
     d = workloads.ptb_inputs(cfg, device="cuda")
     host = {k: v.cpu() for k, v in d.items()}

@@ -234,9 +234,31 @@ def check_row_sampling():
                        atol=1e-13)
 
 
+def check_linear_slabs():
+    """oracle.linear upcasts the weight a slab of 8192 output rows at a time.
+    A selector weight pins every output column by a closed form: row r of w
+    is (r + 1) times the unit vector e_(r mod K), so y[..., r] = (r + 1) *
+    a[..., r mod K] exactly (every other product is an exact zero).  With
+    2 * 8192 + 37 rows the check spans two full slabs and a ragged third, and
+    a bf16 weight takes the torch upcast path."""
+    k = 24
+    n = 2 * 8192 + 37
+    rng = np.random.default_rng(5)
+    a = rng.standard_normal((2, 3, k))
+    r = np.arange(n)
+    w = np.zeros((n, k))
+    w[r, r % k] = r + 1.0
+    want = a[..., r % k] * (r + 1.0)
+    assert np.array_equal(oracle.linear(a, w), want)
+    wb = torch.from_numpy(w).to(torch.bfloat16)  # r + 1 <= 256 is exact in bf16
+    small = w[:256]
+    assert np.array_equal(oracle.linear(a, wb[:256]), a[..., np.arange(256) % k] * (np.arange(256) + 1.0))
+    assert np.array_equal(oracle.linear(a, small), want[..., :256])
+
+
 # ----------------------------------------------------------------- tests --
 
-CHECKS = [check_counts_closed_form, check_window1_is_v, check_full_causal_vs_sdpa,
+CHECKS = [check_linear_slabs, check_counts_closed_form, check_window1_is_v, check_full_causal_vs_sdpa,
           check_band_vs_sdpa, check_convex_rows, check_layer_norm, check_gelu,
           check_brute_force_ptb, check_brute_force_swa, check_brute_force_serial,
           check_ptb_special_cases,
@@ -313,6 +335,16 @@ def _bad_attn_transposed_wo(u_q, u_k, w_qkv, w_o, heads, window, q_pos, k_pos):
 
 _ORIG_ATTN = ptb_oracle.attention_branch
 
+
+def _bad_linear_drops_ragged_slab(a, w):
+    a = np.asarray(a, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    out = np.zeros(a.shape[:-1] + (w.shape[0],))
+    step = 8192
+    for r0 in range(0, w.shape[0] // step * step, step):
+        out[..., r0:r0 + step] = a @ w[r0:r0 + step].T
+    return out
+
 MUTATIONS = [
     ("band_mask", _bad_mask_off_by_one, check_counts_closed_form),
     ("band_mask", _bad_mask_off_by_one, check_band_vs_sdpa),
@@ -322,6 +354,7 @@ MUTATIONS = [
     ("mlp_branch", _bad_mlp_dropped, check_brute_force_ptb),
     ("mlp_branch", _bad_mlp_dropped, check_brute_force_serial),
     ("attention_branch", _bad_attn_transposed_wo, check_brute_force_ptb),
+    ("linear", _bad_linear_drops_ragged_slab, check_linear_slabs),
 ]
 
 

@@ -54,3 +54,15 @@ def test_e4m3_codes_known_values():
     # 17 lies halfway between the e4m3 values 16 and 18 and goes to 16.
     codes, s = e4m3_codes_fp32(torch.tensor([[896.0, 34.0]]))
     assert s.tolist() == [2.0] and codes[0].tolist() == [0x7E, 0x58]
+
+
+def test_e4m3_linear_slabs_equal_whole():
+    """The FP8 storage model quantizes weights a slab of rows at a time; with
+    per-row scales that is the same as quantizing the whole matrix."""
+    from tests.bf16_storage_model import _e4m3_linear, e4m3_rows
+    rng = np.random.default_rng(3)
+    a = rng.standard_normal((5, 40))
+    w = rng.standard_normal((23, 40)) * np.linspace(0.01, 3.0, 23)[:, None]
+    whole = a @ e4m3_rows(w).T
+    assert np.array_equal(_e4m3_linear(a, w, slab=4), whole)
+    assert np.array_equal(_e4m3_linear(a, torch.from_numpy(w), slab=100), whole)
