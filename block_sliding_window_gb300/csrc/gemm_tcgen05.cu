@@ -26,7 +26,8 @@
 //
 // Work units.  The tiles that fill whole waves (a multiple of the grid) are
 // processed whole, M-fastest, so the M tiles of one weight block run at the
-// same time and share it through L2.  The remaining R < grid tiles of the
+// same time and share it through L2; odd waves walk K backwards, so each wave
+// starts on the k-slabs the previous one left in L2.  The remaining R < grid tiles of the
 // last, partial wave are each split along K into S pieces (R*S <= grid), one
 // piece per otherwise idle CTA.  A piece writes its fp32 partial tile to the
 // workspace and bumps an arrival counter per 32-row quarter of the tile; the
@@ -114,6 +115,16 @@ __device__ __forceinline__ bool unit_at(const GemmArgs& p, int num_tiles, int nu
     return true;
   }
   return false;
+}
+
+// The t-th k-block a unit processes.  Whole-tile units of odd waves (odd
+// unit index i) walk K backwards: a wave's tiles read the shared operand
+// k-slab by k-slab in step, and the operand of the long-K GEMMs is larger
+// than L2, so a wave that starts where the previous one ended finds its
+// first k-slabs still in L2 instead of re-reading them from DRAM.  K pieces
+// of split tiles keep the forward order.
+__device__ __forceinline__ int unit_kb(const Unit& u, int i, int t) {
+  return ((i & 1) && u.slot < 0) ? u.kb1 - 1 - t : u.kb0 + t;
 }
 
 // e4m3 operands carry one scale per A row and one per B row (= output
@@ -429,7 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         tile_origin(p, u.tile, num_m, num_n, BM, BN, m0, n0);
         const bool nlo = n0 < p.n_split;
         const int by = nlo ? n0 : n0 - p.n_split;
-        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+        for (int t = 0; t < u.kb1 - u.kb0; ++t) {
+          const int kb = unit_kb(u, i, t);
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
@@ -488,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+        for (int t = 0; t < u.kb1 - u.kb0; ++t) {
           if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status)) {
             ok = false;
             break;
@@ -505,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           constexpr uint64_t kStepB = kBmn ? 128 : 2;
 #pragma unroll
           for (int kk = 0; kk < kMmasPerBlock; ++kk) {
-            const uint32_t accum = (kb != u.kb0 || kk != 0) ? 1u : 0u;
+            const uint32_t accum = (t != 0 || kk != 0) ? 1u : 0u;
             if constexpr (FP8)
               umma_e4m3_ss(d_tmem, adesc + kStepA * kk, bdesc + kStepB * kk, idesc, accum);
             else
@@ -682,7 +694,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bool nlo = n0 < p.n_split;
         const int by = (nlo ? n0 : n0 - p.n_split) + static_cast<int>(rank) * (BN / 2);
         const int my_m = m0 + static_cast<int>(rank) * BM;
-        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+        for (int t = 0; t < u.kb1 - u.kb0; ++t) {
+          const int kb = unit_kb(u, i, t);
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
@@ -752,7 +765,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+        for (int t = 0; t < u.kb1 - u.kb0; ++t) {
           if (!mbar_wait_cluster(&full_bar[stage], phase, abort_flag, p.status)) {
             ok = false;
             break;
@@ -764,7 +777,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                       : sw128_kmajor_desc(smem_addr(stage_b(stage)));
 #pragma unroll
           for (int kk = 0; kk < kMmasPerBlock; ++kk) {
-            const uint32_t accum = (kb != u.kb0 || kk != 0) ? 1u : 0u;
+            const uint32_t accum = (t != 0 || kk != 0) ? 1u : 0u;
             if constexpr (FP8)
               umma_e4m3_pair(d_tmem, adesc + kStepA * kk, bdesc + kStepB * kk, idesc, accum);
             else
