@@ -40,7 +40,10 @@
 //               from (row = lane, two keys per column), where the P V MMA
 //               reads it as its A operand: P never passes through shared
 //               memory, and a softmax warp waits for a P V only to rescale O.
-//               At the end of an item O / l -> bf16.
+//               At the end of an item O / l -> bf16, staged per warp in 4 KB
+//               of shared memory (32 rows x 64 columns) and written with a TMA
+//               store: 55.6 -> 52.5 us on the operator, against 16-byte
+//               stores from registers (each warp store then touched 32 rows).
 // Every mbarrier wait is bounded (see mbar_wait); on a timeout all roles
 // unwind, wait for their own copies and MMAs, free TMEM and return.
 #include "ptb_device.cuh"
@@ -60,7 +63,9 @@ struct SwaCfg {
   static constexpr int kQTileBytes = kAtoms * BQ * 128;
   static constexpr int kKVBytes = kAtoms * BKV * 128;   // one of K or V, one stage
   // P never touches shared memory: it overwrites its own score buffer in TMEM.
-  static constexpr int kFixed = QT * kQTileBytes + 512 + 1024;
+  // Output staging: one 32-row x 64-column block (4 KB) per softmax warp.
+  static constexpr int kOStageBytes = 32 * 128;
+  static constexpr int kFixed = QT * kQTileBytes + 4 * QT * kOStageBytes + 512 + 1024;
   static constexpr int kNSFit = (227 * 1024 - kFixed) / (2 * kKVBytes);
   static constexpr int kNS = kNSFit < 6 ? kNSFit : 6;  // K/V stages
   static constexpr int kSmemBytes = kFixed + kNS * 2 * kKVBytes;
@@ -71,6 +76,8 @@ struct SwaCfg {
 
 struct SwaParams {
   CUtensorMap tq, tk, tv;  // 4-D maps {d, dim1, dim2, batch}; boxes {64, ., ., 1}
+  CUtensorMap to;          // the output, boxes of 64 columns x 32 rows
+  int o_seq_dim;           // which dimension of `to` is the sequence
   SwaArgs a;
   int seq_dim;             // 1 or 2: which map dimension is the sequence
   int num_items, q_blocks;
@@ -125,7 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
   uint8_t* sQ = smem;                               // [QT][kQTileBytes]
   uint8_t* sK = sQ + QT * C::kQTileBytes;           // [NS][kKVBytes]
   uint8_t* sV = sK + NS * C::kKVBytes;              // [NS][kKVBytes]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NS * C::kKVBytes);
+  uint8_t* sO = sV + NS * C::kKVBytes;              // [4 * QT][kOStageBytes]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sO + 4 * QT * C::kOStageBytes);
   uint64_t* q_full = bars;
   uint64_t* q_empty = q_full + 1;
   uint64_t* kv_full = q_empty + 1;      // [NS]
@@ -467,36 +475,48 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
         break;
       }
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      __nv_bfloat16* orow =
-          a.o + it.b * a.o_sb + it.h * a.o_sh + static_cast<int64_t>(i < a.seq ? i : 0) * a.o_ss;
-      if constexpr (D % 32 == 0) {
+      // O / l as bf16, one 64-column block at a time: each warp writes its 32
+      // rows into its own 4 KB of shared memory in the 128-byte-swizzled
+      // layout of the output tensor map (16-byte chunk c of row r at
+      // r * 128 + ((c ^ (r % 8)) * 16)), and its lane 0 stores the block
+      // with TMA (rows past the sequence and columns past d are not
+      // written).  One 32-row TMA store replaces 256 scattered 16-byte stores
+      // (32 rows x 8 chunks) per block and warp.
+      uint8_t* stage = sO + (x * 4 + quarter) * C::kOStageBytes;
+      constexpr int kCols = D < 32 ? D : 32;  // columns per TMEM load
 #pragma unroll
-        for (int c = 0; c < D; c += 32) {
+      for (int at = 0; at < C::kAtoms; ++at) {
+        // The previous block (of this item or the last one) has left shared memory.
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+#pragma unroll
+        for (int c = at * 64; c < min(D, at * 64 + 64); c += kCols) {
           uint32_t o[32];
-          tmem_ld_32x32b_x32(o_tmem + c, o);
+          if constexpr (kCols == 32)
+            tmem_ld_32x32b_x32(o_tmem + c, o);
+          else
+            tmem_ld_32x32b_x16(o_tmem + c, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
           tmem_ld_wait();
-          if (i < a.seq) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 8)
-              *reinterpret_cast<uint4*>(orow + c + e) = make_uint4(
-                  pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
-                  pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
-                  pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
-                  pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+          for (int e = 0; e < kCols; e += 8) {
+            const int chunk = ((c % 64) + e) / 8;
+            *reinterpret_cast<uint4*>(stage + lane * 128 + ((chunk ^ (lane & 7)) << 4)) =
+                make_uint4(
+                    pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
+                    pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
+                    pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
+                    pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
           }
         }
-      } else {
-        uint32_t o[16];
-        tmem_ld_32x32b_x16(o_tmem, o);
-        tmem_ld_wait();
-        if (i < a.seq) {
-#pragma unroll
-          for (int e = 0; e < 16; e += 8)
-            *reinterpret_cast<uint4*>(orow + e) = make_uint4(
-                pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
-                pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
-                pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
-                pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int row0 = it.q0 + x * BQ + quarter * 32;
+          if (P.o_seq_dim == 2)
+            tma_store_4d(&P.to, stage, at * 64, it.h, row0, it.b);
+          else
+            tma_store_4d(&P.to, stage, at * 64, row0, it.h, it.b);
+          bulk_commit_group();
         }
       }
       tc_fence_before();
@@ -506,6 +526,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_tc_kernel(const __grid_consta
       if (a.lse && i < a.seq)
         a.lse[(static_cast<int64_t>(it.b) * a.heads + it.h) * a.seq + i] = m_ref + log2f(l_run);
     }
+    // The output stores this warp issued complete before the CTA ends.
+    if (lane == 0) bulk_wait_all();
   }
 
   __syncwarp();
@@ -585,6 +607,10 @@ cudaError_t launch_swa(const SwaArgs& a, cudaStream_t stream) {
       !swa_map(&prm.tv, a.v, bstride(a.v_sb, a.v_sh, a.v_ss), a.v_sh, a.v_ss, a, BKV, &sd_v))
     return cudaErrorInvalidValue;
   if (sd_q != sd_k || sd_q != sd_v) return cudaErrorInvalidValue;
+  int sd_o = 0;
+  if (!swa_map(&prm.to, a.o, bstride(a.o_sb, a.o_sh, a.o_ss), a.o_sh, a.o_ss, a, 32, &sd_o))
+    return cudaErrorInvalidValue;
+  prm.o_seq_dim = sd_o;
   prm.seq_dim = sd_q;
   prm.q_blocks = (a.seq + QT * BQ - 1) / (QT * BQ);
   const int64_t items = static_cast<int64_t>(prm.q_blocks) * a.heads * a.batch;
