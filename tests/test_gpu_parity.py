@@ -202,6 +202,27 @@ def test_swa_strided_in_place(ptb_lib):
     assert torch.equal(u[:, :, hdim:], untouched), "SWA wrote outside its output block"
 
 
+@pytest.mark.parametrize("d,w", [(96, 77), (128, 300), (32, 50)])
+def test_swa_output_layout_differs_from_inputs(ptb_lib, d, w):
+    """Q, K, V as head-strided column blocks of a [B, s, 3H + 8] buffer and
+    the output in its own [B, heads, s, d] buffer with a padded row stride:
+    the output tensor map has the other dimension order and strides than
+    the input maps, and ragged rows past the sequence must not be written."""
+    b, s, nh = 2, 300, 3
+    hdim = nh * d
+    ld = 3 * hdim + 8
+    u = workloads.normal_bf16((b, s, ld), seed=d + w).cuda()
+    view = lambda off: u[:, :, off:off + hdim].unflatten(2, (nh, d)).transpose(1, 2)  # noqa: E731
+    q, k, v = view(0), view(hdim), view(2 * hdim)
+    pad = 8
+    big = torch.full((b, nh, s + 1, d + pad), 7.0, dtype=torch.bfloat16, device="cuda")
+    o = big[:, :, :s, :d]  # row stride d + pad, head stride (s + 1)(d + pad)
+    ptb_lib.swa_attention_strided(q, k, v, o, w)
+    assert_close(o, oracle.swa(q.cpu(), k.cpu(), v.cpu(), w), f"SWA d={d} w={w}, separate output")
+    assert bool((big[:, :, s, :] == 7.0).all()), "a row past the sequence was written"
+    assert bool((big[:, :, :, d:] == 7.0).all()), "columns past d were written"
+
+
 # ---------------------------------------------------------------- PTB layer --
 
 SMALL_LAYERS = [
