@@ -35,6 +35,9 @@ struct DeviceState {
   unsigned* status_taken = nullptr;
   void* arena = nullptr;
   size_t arena_bytes = 0;
+  // Recorded after the layer of the latest ptb_forward_host call, so that
+  // the next call's layer (possibly on another stream) runs after it.
+  cudaEvent_t host_layer_done = nullptr;
 };
 
 // Per-device set-up on first use (SM count, status word, architecture check,
