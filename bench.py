@@ -353,16 +353,17 @@ def run_train(args, world, rank, local):
     w = (d["w_qkv"], d["w_o"], d["w_up"], d["w_down"])
     stream = torch.cuda.current_stream()
 
-    def step(x_in, dy_in, marks=None):
+    def step(x_in, dy_in, marks=None, g=None):
+        g = grads if g is None else g
         if marks is not None:
             marks[0].record(stream)
         bsw.ptb_forward_train(x_in, d["ln_gamma"], d["ln_beta"], *w, cfg.heads, cfg.window, y=y,
                               saved=saved, workspace=ws_f)
         if marks is not None:
             return bsw.ptb_backward_events(dy_in, x_in, d["ln_gamma"], *w, saved, cfg.heads,
-                                           cfg.window, marks[1:], grads=grads, workspace=ws_b)
+                                           cfg.window, marks[1:], grads=g, workspace=ws_b)
         return bsw.ptb_backward(dy_in, x_in, d["ln_gamma"], *w, saved, cfg.heads, cfg.window,
-                                grads=grads, workspace=ws_b)
+                                grads=g, workspace=ws_b)
 
     for _ in range(args.warmup):
         step(d["x"], dy)
@@ -392,24 +393,47 @@ def run_train(args, world, rank, local):
     # End to end through the public calls: x and dy in from pinned host
     # memory, dx out, every step (the weight gradients stay on the device
     # for the optimizer).
+    # The steps run in order on the launching stream; step i's copies run on
+    # copy stream i % 2 into and out of buffers of their own, so one step's
+    # copies overlap the neighbouring steps' kernels.
     x_host, dy_host = d["x"].cpu().pin_memory(), dy.cpu().pin_memory()
     dx_host = torch.empty(d["x"].shape, dtype=torch.bfloat16, pin_memory=True)
-    x_dev, dy_dev = torch.empty_like(d["x"]), torch.empty_like(dy)
-    for _ in range(max(1, args.warmup)):
-        x_dev.copy_(x_host, non_blocking=True)
-        dy_dev.copy_(dy_host, non_blocking=True)
-        step(x_dev, dy_dev)
-        dx_host.copy_(grads["dx"], non_blocking=True)
+    dx_hosts = [dx_host, torch.empty(d["x"].shape, dtype=torch.bfloat16, pin_memory=True)]
+    x_devs = [torch.empty_like(d["x"]) for _ in range(2)]
+    dy_devs = [torch.empty_like(dy) for _ in range(2)]
+    g_bufs = [grads, dict(grads, dx=torch.empty_like(d["x"]))]
+    copy_streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+
+    def copied_step(i):
+        cs = copy_streams[i % 2]
+        with torch.cuda.stream(cs):
+            x_devs[i % 2].copy_(x_host, non_blocking=True)
+            dy_devs[i % 2].copy_(dy_host, non_blocking=True)
+            ready = torch.cuda.Event()
+            ready.record(cs)
+        stream.wait_event(ready)
+        step(x_devs[i % 2], dy_devs[i % 2], g=g_bufs[i % 2])
+        done = torch.cuda.Event()
+        done.record(stream)
+        cs.wait_event(done)
+        with torch.cuda.stream(cs):
+            dx_hosts[i % 2].copy_(g_bufs[i % 2]["dx"], non_blocking=True)
+
+    for i in range(max(2, args.warmup)):
+        copied_step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(args.steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        dy_dev.copy_(dy_host, non_blocking=True)
-        step(x_dev, dy_dev)
-        dx_host.copy_(grads["dx"], non_blocking=True)
+    for cs in copy_streams:
+        cs.wait_event(e0)
+    for i in range(args.steps):
+        copied_step(i)
+    for cs in copy_streams:
+        fin = torch.cuda.Event()
+        fin.record(cs)
+        stream.wait_event(fin)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -486,19 +510,21 @@ def run_ours(args, world, rank, local):
                 d["w_down"], cfg.heads, cfg.window)
     stream = torch.cuda.current_stream()
 
-    def layer(x_in, marks=None):
+    def layer(x_in, marks=None, y_out=None):
+        y_out = y if y_out is None else y_out
         if fp8:
             if marks is not None:
                 return bsw.ptb_forward_fp8_events(x_in, d["ln_gamma"], d["ln_beta"], w8,
-                                                  cfg.heads, cfg.window, marks, y=y, workspace=ws)
+                                                  cfg.heads, cfg.window, marks, y=y_out,
+                                                  workspace=ws)
             return bsw.ptb_forward_fp8(x_in, d["ln_gamma"], d["ln_beta"], w8, cfg.heads,
-                                       cfg.window, y=y, workspace=ws)
+                                       cfg.window, y=y_out, workspace=ws)
         if serial:  # second LayerNorm: gamma = 1, beta = 0 like the first
             return bsw.serial_forward(x_in, d["ln_gamma"], d["ln_beta"], d["ln_gamma"],
-                                      d["ln_beta"], *fwd_args[3:], y=y, workspace=ws)
+                                      d["ln_beta"], *fwd_args[3:], y=y_out, workspace=ws)
         if marks is not None:
-            return bsw.ptb_forward_events(x_in, *fwd_args[1:], marks, y=y, workspace=ws)
-        return bsw.ptb_forward(x_in, *fwd_args[1:], y=y, workspace=ws)
+            return bsw.ptb_forward_events(x_in, *fwd_args[1:], marks, y=y_out, workspace=ws)
+        return bsw.ptb_forward(x_in, *fwd_args[1:], y=y_out, workspace=ws)
 
     for _ in range(args.warmup):
         layer(d["x"])
@@ -573,19 +599,42 @@ def run_ours(args, world, rank, local):
             stream.wait_event(done)
         e1.record(stream)
     else:
-        x_dev = torch.empty_like(d["x"])
-        for _ in range(max(1, args.warmup)):
-            x_dev.copy_(x_host, non_blocking=True)
-            layer(x_dev)
-            y_host.copy_(y, non_blocking=True)
+        # The layers run in order on the launching stream; step i's copies
+        # run on copy stream i % 2 into and out of buffers of their own, so
+        # one step's copies overlap the neighbouring steps' layers.
+        x_devs = [torch.empty_like(d["x"]) for _ in range(2)]
+        y_devs = [torch.empty_like(d["x"]) for _ in range(2)]
+        y_hosts = [y_host, torch.empty(d["x"].shape, dtype=torch.bfloat16, pin_memory=True)]
+        copy_streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+
+        def copied_step(i):
+            cs = copy_streams[i % 2]
+            with torch.cuda.stream(cs):
+                x_devs[i % 2].copy_(x_host, non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(cs)
+            stream.wait_event(ready)
+            layer(x_devs[i % 2], y_out=y_devs[i % 2])
+            done = torch.cuda.Event()
+            done.record(stream)
+            cs.wait_event(done)
+            with torch.cuda.stream(cs):
+                y_hosts[i % 2].copy_(y_devs[i % 2], non_blocking=True)
+
+        for i in range(max(2, args.warmup)):
+            copied_step(i)
         torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
         e0.record(stream)
-        for _ in range(args.steps):
-            x_dev.copy_(x_host, non_blocking=True)
-            layer(x_dev)
-            y_host.copy_(y, non_blocking=True)
+        for cs in copy_streams:
+            cs.wait_event(e0)
+        for i in range(args.steps):
+            copied_step(i)
+        for cs in copy_streams:
+            fin = torch.cuda.Event()
+            fin.record(cs)
+            stream.wait_event(fin)
         e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
