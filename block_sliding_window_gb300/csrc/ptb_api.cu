@@ -706,6 +706,24 @@ size_t ptb_forward_host_workspace_size(int64_t batch, int64_t seq, int64_t hidde
   return 2 * round_up(t * hidden * 2, kAlign) + layer;
 }
 
+namespace {
+// The rest of ptb_forward_host for a layer that does not wait: the layer and
+// the copy of y back, on `stream`.
+ptb_status forward_host_tail(const ptb_bf16* x_dev, ptb_bf16* y_dev, ptb_bf16* y_host,
+                             size_t bytes, const ptb_bf16* ln_gamma, const ptb_bf16* ln_beta,
+                             const ptb_bf16* w_qkv, const ptb_bf16* w_o, const ptb_bf16* w_up,
+                             const ptb_bf16* w_down, int64_t batch, int64_t seq, int64_t hidden,
+                             int64_t ffn, int32_t heads, int32_t window, void* layer_ws,
+                             size_t layer_bytes, cudaStream_t stream) {
+  ptb_status st = ptb_forward(x_dev, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, batch, seq,
+                              hidden, ffn, heads, window, y_dev, layer_ws, layer_bytes, stream);
+  if (st != PTB_OK) return st;
+  if (cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return PTB_ERR_LAUNCH;
+  return PTB_OK;
+}
+}  // namespace
+
 ptb_status ptb_forward_host(const ptb_bf16* x_host, const ptb_bf16* ln_gamma,
                             const ptb_bf16* ln_beta, const ptb_bf16* w_qkv, const ptb_bf16* w_o,
                             const ptb_bf16* w_up, const ptb_bf16* w_down, int64_t batch,
@@ -729,12 +747,21 @@ ptb_status ptb_forward_host(const ptb_bf16* x_host, const ptb_bf16* ln_gamma,
   if (st != PTB_OK) return st;
   if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
     return PTB_ERR_LAUNCH;
+  // The layer's kernels are persistent and take every SM.  For large layers
+  // two layers in flight at once only fight over the SMs (175B-class: two
+  // streams of layers 5.10 ms per layer, one stream 4.77-4.89 ms), so the
+  // layer waits for the previous large call's layer, whatever its stream,
+  // while the copies of one call still overlap the other call's layer.
+  // Small layers gain from running side by side (13B-class: 2.50 M tokens/s
+  // with two streams of calls, 2.32 M serialised), so they do not wait.  The
+  // line is the CTA-pair rule's: a first GEMM of more than 2^39 multiply-adds.
+  const bool serialise = static_cast<double>(batch) * seq * hidden * (3.0 * hidden + ffn) >
+                         549755813888.0;
+  if (!serialise)
+    return forward_host_tail(x_dev, y_dev, y_host, bytes, ln_gamma, ln_beta, w_qkv, w_o, w_up,
+                             w_down, batch, seq, hidden, ffn, heads, window, layer_ws,
+                             layer_bytes, stream);
   {
-    // The layer's kernels are persistent and take every SM: two layers in
-    // flight at once only fight over the SMs (measured at 175B: two streams
-    // of layers 5.10 ms per layer, one stream 4.77-4.89 ms).  So each call's
-    // layer waits for the previous call's layer, whatever its stream, while
-    // the copies of one call still overlap the other call's layer.
     std::lock_guard<std::mutex> lock(g_host_mutex);
     if (!ds->host_layer_done &&
         cudaEventCreateWithFlags(&ds->host_layer_done, cudaEventDisableTiming) != cudaSuccess) {
@@ -743,7 +770,7 @@ ptb_status ptb_forward_host(const ptb_bf16* x_host, const ptb_bf16* ln_gamma,
     }
     if (cudaStreamWaitEvent(stream, ds->host_layer_done, 0) != cudaSuccess) return PTB_ERR_LAUNCH;
     st = ptb_forward(x_dev, ln_gamma, ln_beta, w_qkv, w_o, w_up, w_down, batch, seq, hidden, ffn,
-                     heads, window, y_dev, layer_ws, layer_bytes, stream_);
+                     heads, window, y_dev, layer_ws, layer_bytes, stream);
     if (st != PTB_OK) return st;
     if (cudaEventRecord(ds->host_layer_done, stream) != cudaSuccess) return PTB_ERR_LAUNCH;
   }

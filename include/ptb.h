@@ -130,10 +130,12 @@ ptb_status ptb_forward_events(const ptb_bf16* x, const ptb_bf16* ln_gamma,
  * caller-owned device memory of ptb_forward_host_workspace_size bytes
  * (256-byte aligned; not null), holding the device copies of x and y and
  * the layer's scratch; calls in flight at the same time need separate
- * workspaces.  The layer of each call runs after the layer of the previous
- * call on the same device, whatever its stream (the kernels take every SM,
- * so two layers at once would only compete), while the copies of calls on
- * different streams overlap the other calls' layers.  Errors as ptb_forward.
+ * workspaces.  For layers whose first GEMM exceeds 2^39 multiply-adds the
+ * layer of each call runs after the layer of the previous such call on the
+ * same device, whatever its stream (the kernels take every SM, so two large
+ * layers at once only compete), while the copies of calls on different
+ * streams overlap the other calls' layers; smaller layers of calls on
+ * different streams may run side by side.  Errors as ptb_forward.
  */
 size_t ptb_forward_host_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn);
 ptb_status ptb_forward_host(const ptb_bf16* x_host, const ptb_bf16* ln_gamma,
