@@ -303,10 +303,54 @@ def run_swa(args, world, rank, local):
         evs[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    clk = clocks.stop()
     per_step = [a.elapsed_time(b) for a, b in evs]
     kern_ms = sum(per_step) / args.steps
     ms = max_over_ranks(kern_ms, world)
+
+    # End to end: q, k and v in from pinned host memory and o out, every
+    # step.  Step i's copies run on copy stream i % 2 into and out of device
+    # buffers of their own, so one step's copies overlap the neighbouring
+    # steps' kernels.
+    hosts = [t.cpu().pin_memory() for t in (q, k, v)]
+    o_hosts = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
+    bufs = [[torch.empty_like(q) for _ in range(4)] for _ in range(2)]  # q, k, v, o
+    copy_streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+
+    def copied_step(i):
+        cs, b = copy_streams[i % 2], bufs[i % 2]
+        with torch.cuda.stream(cs):
+            for dst, src in zip(b[:3], hosts):
+                dst.copy_(src, non_blocking=True)
+            ready = torch.cuda.Event()
+            ready.record(cs)
+        stream.wait_event(ready)
+        bsw.swa_attention(b[0], b[1], b[2], cfg.window, o=b[3])
+        done = torch.cuda.Event()
+        done.record(stream)
+        cs.wait_event(done)
+        with torch.cuda.stream(cs):
+            o_hosts[i % 2].copy_(b[3], non_blocking=True)
+
+    for i in range(max(2, args.warmup)):
+        copied_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for cs in copy_streams:
+        cs.wait_event(e0)
+    for i in range(args.steps):
+        copied_step(i)
+    for cs in copy_streams:
+        fin = torch.cuda.Event()
+        fin.record(cs)
+        stream.wait_event(fin)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
     band = sum(min(i + 1, cfg.window) for i in range(cfg.seq))
     tokens = cfg.batch * cfg.seq
     flops = swa_flops(cfg)
@@ -327,6 +371,8 @@ def run_swa(args, world, rank, local):
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": ach / peaks["hbm_gbs"], "peak_source": peak_src,
                          "traffic": traffic_for("swa_kernel", "swa", SWA_SRC)},
+            "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": o.numel() * 2},
             "clocks": clk, "gpu_launches": args.steps}), flush=True)
 
 
