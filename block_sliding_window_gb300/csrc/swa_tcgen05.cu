@@ -11,7 +11,7 @@
 // every K/V tile.  416 threads:
 //   warp 0      TMA: the two Q tiles of an item, then the 64-key K and V
 //               tiles intersecting the item's band [q0 - w + 1, q0 + 255]
-//               (diagonal tile first) into a ring of 5 stages (d > 64; 6 for
+//               (diagonal tile first) into a ring of 4 stages (d > 64; 6 for
 //               d <= 64) that runs on across items.  d < 128 is read as
 //               64-wide boxes; columns past d are zero-filled by TMA.  (An L2
 //               prefetch of the tiles four positions ahead was measured
