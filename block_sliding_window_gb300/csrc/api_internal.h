@@ -83,15 +83,14 @@ GemmSpec spec_out_down(const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16* g, i
 ptb_status gemm_run(DeviceState* ds, const GemmSpec& g, int64_t tokens, ptb_bf16* out, int64_t ldo,
                     const ptb_bf16* resid, int64_t ldr, int64_t gelu_col, void* scratch,
                     size_t scratch_bytes, cudaStream_t stream, ptb_bf16* aux = nullptr,
-                    int64_t ld_aux = 0, bool training = false);
+                    int64_t ld_aux = 0);
 ptb_status gemm_qkv_up(DeviceState* ds, const ptb_bf16* xn, const ptb_bf16* w_qkv,
                        const ptb_bf16* w_up, int64_t tokens, int64_t hidden, int64_t ffn,
                        ptb_bf16* u, void* scratch, size_t scratch_bytes, cudaStream_t stream);
 ptb_status gemm_out_down(DeviceState* ds, const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16* g,
                          int64_t ld_g, const ptb_bf16* w_o, const ptb_bf16* w_down,
                          const ptb_bf16* x, int64_t tokens, int64_t hidden, int64_t ffn,
-                         ptb_bf16* y, void* scratch, size_t scratch_bytes, cudaStream_t stream,
-                         bool training = false);
+                         ptb_bf16* y, void* scratch, size_t scratch_bytes, cudaStream_t stream);
 
 // A GEMM of the backward pass, C[M, N] = A[M, K] B[N, K]^T, with operands
 // read in place from row-major matrices:

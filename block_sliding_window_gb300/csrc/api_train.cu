@@ -200,7 +200,7 @@ ptb_status ptb_forward_train(const ptb_bf16* x, const ptb_bf16* ln_gamma, const 
     return PTB_ERR_LAUNCH;
   // 2. U = [xn W_qkv^T | gelu(Z)], Z = xn W_up^T kept
   st = gemm_run(ds, spec_qkv_up(xn, w_qkv, w_up, hidden, ffn), tokens, u, ldu, nullptr, 0,
-                3 * hidden, workspace, need, stream, z, ffn, true);
+                3 * hidden, workspace, need, stream, z, ffn);
   if (st != PTB_OK) return st;
   // 3. ctx = SWA(Q, K, V) into its own buffer (Q is needed again), with the
   //    per-row log-sum-exp
@@ -212,7 +212,7 @@ ptb_status ptb_forward_train(const ptb_bf16* x, const ptb_bf16* ln_gamma, const 
   if (launch_swa(sa, stream) != cudaSuccess) return PTB_ERR_LAUNCH;
   // 4. y = x + [ctx | G] [W_o | W_down]^T
   return gemm_out_down(ds, ctx, hidden, u + 3 * hidden, ldu, w_o, w_down, x, tokens, hidden, ffn,
-                       y, workspace, need, stream, true);
+                       y, workspace, need, stream);
 }
 
 size_t ptb_backward_workspace_size(int64_t batch, int64_t seq, int64_t hidden, int64_t ffn,

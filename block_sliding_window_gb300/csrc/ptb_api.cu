@@ -109,24 +109,20 @@ size_t gemm_scratch_bytes(const GemmPlan& g) {
   return round_up(g.partial_bytes, kAlign) + round_up(g.counter_bytes, kAlign);
 }
 
-// Whether a GEMM that can run on CTA pairs does.  Automatic mode: always in
-// a training step (ptb_forward_train, ptb_backward); in a forward-only call
-// only for GEMMs of at most 2^39 multiply-adds.  Measured on GB300: pairs do
-// a k-block in ~28% fewer cycles.  That made the 13B-class forward layer
-// (GEMMs of 3.8e11 and 2.7e11 multiply-adds) 9% faster at an unchanged
-// 2070 MHz, and the training step 6% faster at both 13B and 175B.  Back-to-
-// back 175B- and 530B-class forward layers (2.2e12 / 1.5e12 and 6.9e12 /
-// 5.2e12) run at the 1.4 kW power cap, where pairs ran their GEMMs no
-// faster, at 1500 instead of 1920 MHz, which then also slowed the attention
-// and LayerNorm kernels: the forward layer took 0.4-1.2% longer.  The e4m3
-// layer behaves alike: pairs took 5% off the 13B-class layer, nothing at 175B
-// (its GEMM holds 3.1 PFLOP/s at 2070 MHz either way) and added 3% at 530B.
-bool use_pairs(const DeviceState* ds, bool shape_ok, int64_t m, int64_t n, int64_t k,
-               bool training) {
-  if (!shape_ok || m <= 128 || ds->sms < 2 || ds->pairs == 0) return false;
-  if (ds->pairs == 1 || training) return true;
-  return static_cast<double>(m) * static_cast<double>(n) * static_cast<double>(k) <=
-         549755813888.0;
+// Whether a GEMM that can run on CTA pairs does: always, unless pairs are
+// switched off (ptb_set_gemm_pairs(0)).  Measured on GB300: pairs do a
+// k-block in ~28% fewer cycles.  That made the 13B-class forward layer 9%
+// faster at an unchanged 2070 MHz and the training step 6% faster at 13B and
+// 175B.  Back-to-back 175B- and 530B-class forward layers run at the 1.4 kW
+// power cap; there pairs first looked no faster (the clock fell from 1.92 to
+// 1.5 GHz), but that was with the weights loaded evict_first, which left the
+// pair kernel re-reading them from DRAM (6.1-6.5 GB per launch of the
+// 175B-class [out | down] GEMM, 3.2 GB with evict_last).  With both operands
+// evict_last, pairs for both GEMMs against single CTAs: 175B class 4.45 vs
+// 4.58 ms, 530B class 12.13-12.18 vs 12.85-12.90 ms, e4m3 175B 2.48-2.53 vs
+// 2.56-2.58 ms, e4m3 530B 6.42-6.47 vs 6.84-6.85 ms.
+bool use_pairs(const DeviceState* ds, bool shape_ok, int64_t m) {
+  return shape_ok && m > 128 && ds->sms >= 2 && ds->pairs != 0;
 }
 
 // Output tiles of a launch: 128-row tiles, or 256-row tiles on CTA pairs.
@@ -191,7 +187,7 @@ size_t spec_scratch(const GemmSpec& g, int64_t tokens, int sms) {
 ptb_status gemm_run(DeviceState* ds, const GemmSpec& g, int64_t tokens, ptb_bf16* out, int64_t ldo,
                     const ptb_bf16* resid, int64_t ldr, int64_t gelu_col, void* scratch,
                     size_t scratch_bytes, cudaStream_t stream, ptb_bf16* aux,
-                    int64_t ld_aux, bool training) {
+                    int64_t ld_aux) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.block_n = g.block_n();
@@ -199,7 +195,7 @@ ptb_status gemm_run(DeviceState* ds, const GemmSpec& g, int64_t tokens, ptb_bf16
   const int64_t K = g.k(), N = g.n();
   // CTA pairs for bf16 GEMMs with 256-wide N tiles and more than one
   // 128-row tile of M; each CTA of a pair loads half of the B tile.
-  a.pair = use_pairs(ds, a.block_n == 256, tokens, N, K, training) ? 1 : 0;
+  a.pair = use_pairs(ds, a.block_n == 256, tokens) ? 1 : 0;
   const uint32_t box_b = a.pair ? a.block_n / 2 : a.block_n;
   bool ok;
   if (g.k1) {
@@ -221,12 +217,18 @@ ptb_status gemm_run(DeviceState* ds, const GemmSpec& g, int64_t tokens, ptb_bf16
   a.k_split = static_cast<int>(g.k1 ? g.k0 : K);
   a.layout = kLayoutKK;
   a.n_fastest = 0;
-  // A is re-read by every wave of N tiles (xn in the first GEMM, [ctx | G]
-  // in the second), so it is kept in L2 ahead of the weights, which each
-  // wave streams once.  (Keeping the second GEMM's A: 530B-class layer 2.5%
-  // faster, 175B-class 0.3%, 13B-class unchanged.)
+  // Both operands are loaded evict_last.  A is re-read by every wave of N
+  // tiles (xn in the first GEMM, [ctx | G] in the second); a weight tile is
+  // read by every M tile of its wave, and loaded evict_first its lines were
+  // often gone before the wave's later tiles got to them: the 175B-class
+  // [out | down] GEMM on CTA pairs read 6.1-6.5 GB from DRAM per launch
+  // (3.2 GB with evict_last) and took 1.81-1.83 instead of 1.71-1.72 ms.
+  // Layers: 175B class 4.71-4.72 -> 4.61-4.62 ms, 530B class 13.04-13.06 ->
+  // 12.86-12.89, 13B class 0.827 -> 0.819-0.824, e4m3 175B class 2.64-2.65
+  // -> 2.58-2.61.  (Keeping A alone, against streaming both, had made the
+  // 530B-class layer 2.5% faster.)
   a.a_keep = 1;
-  a.b_keep = 0;
+  a.b_keep = 1;
   a.out = bf(out);
   a.ld_out = ldo;
   a.out1 = a.out;
@@ -270,10 +272,9 @@ ptb_status gemm_qkv_up(DeviceState* ds, const ptb_bf16* xn, const ptb_bf16* w_qk
 ptb_status gemm_out_down(DeviceState* ds, const ptb_bf16* ctx, int64_t ld_ctx, const ptb_bf16* g,
                          int64_t ld_g, const ptb_bf16* w_o, const ptb_bf16* w_down,
                          const ptb_bf16* x, int64_t tokens, int64_t hidden, int64_t ffn,
-                         ptb_bf16* y, void* scratch, size_t scratch_bytes, cudaStream_t stream,
-                         bool training) {
+                         ptb_bf16* y, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
   return gemm_run(ds, spec_out_down(ctx, ld_ctx, g, ld_g, w_o, w_down, hidden, ffn), tokens, y,
-                  hidden, x, hidden, hidden, scratch, scratch_bytes, stream, nullptr, 0, training);
+                  hidden, x, hidden, hidden, scratch, scratch_bytes, stream);
 }
 
 
@@ -304,7 +305,7 @@ ptb_status gemm_call(DeviceState* ds, const GemmCall& c, void* scratch, size_t s
   const ptb_bf16* b1 = (c.k_split || c.n_split) ? c.b1 : c.b0;
   const int64_t ldb1 = (c.k_split || c.n_split) ? c.ldb1 : c.ldb0;
   const int64_t ka1 = k1 ? k1 : k0;
-  a.pair = use_pairs(ds, a.block_n == 256, c.M, c.N, c.K, true) ? 1 : 0;
+  a.pair = use_pairs(ds, a.block_n == 256, c.M) ? 1 : 0;
   const uint32_t box_b = a.pair ? a.block_n / 2 : a.block_n;
   bool ok;
   if (amn)
@@ -754,7 +755,7 @@ ptb_status ptb_forward_host(const ptb_bf16* x_host, const ptb_bf16* ln_gamma,
   // while the copies of one call still overlap the other call's layer.
   // Small layers gain from running side by side (13B-class: 2.50 M tokens/s
   // with two streams of calls, 2.32 M serialised), so they do not wait.  The
-  // line is the CTA-pair rule's: a first GEMM of more than 2^39 multiply-adds.
+  // line lies between the two: a first GEMM of more than 2^39 multiply-adds.
   const bool serialise = static_cast<double>(batch) * seq * hidden * (3.0 * hidden + ffn) >
                          549755813888.0;
   if (!serialise)
