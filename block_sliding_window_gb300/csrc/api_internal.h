@@ -113,7 +113,6 @@ struct GemmCall {
   ptb_bf16* aux = nullptr;
   int64_t ld_aux = 0;
   int64_t gelu_col = 0;
-  bool a_keep = false, b_keep = false;
   int block_n() const {
     return n_split ? pick_block_n(n_split, N - n_split) : pick_block_n(N, N);
   }

@@ -48,7 +48,6 @@ GemmCall call_dgrad_out(int64_t t, int64_t h, int64_t f) {  // [dctx | dG] = dy 
   c.M = t, c.N = h + f, c.K = h, c.n_split = h;
   c.lda0 = h, c.ldb0 = h, c.ldb1 = f;
   c.out_split_col = h, c.gelu_col = h;
-  c.a_keep = true;
   return c;
 }
 GemmCall call_wgrad_out(int64_t t, int64_t h, int64_t f, int64_t ldu) {  // dy^T [ctx | G]
@@ -58,7 +57,6 @@ GemmCall call_wgrad_out(int64_t t, int64_t h, int64_t f, int64_t ldu) {  // dy^T
   c.M = h, c.N = h + f, c.K = t, c.n_split = h;
   c.lda0 = h, c.ldb0 = h, c.ldb1 = ldu;
   c.out_split_col = h;
-  c.a_keep = true;
   return c;
 }
 GemmCall call_dgrad_in(int64_t t, int64_t h, int64_t f, int64_t ldu) {  // dU1 [W_qkv ; W_up]
@@ -67,9 +65,6 @@ GemmCall call_dgrad_in(int64_t t, int64_t h, int64_t f, int64_t ldu) {  // dU1 [
   c.epilogue = kEpiF32;
   c.M = t, c.N = h, c.K = ldu, c.k_split = 3 * h;
   c.lda0 = ldu, c.lda1 = ldu, c.ldb0 = h, c.ldb1 = h;
-  // dU1 is re-read by every wave of N tiles, the weights once: keep dU1 in
-  // L2 (175B-class: this GEMM 2.75 -> 2.70 ms).
-  c.a_keep = true;
   (void)f;
   return c;
 }
@@ -80,7 +75,6 @@ GemmCall call_wgrad_in(int64_t t, int64_t h, int64_t f, int64_t ldu) {  // dU1^T
   c.M = ldu, c.N = h, c.K = t;
   c.lda0 = ldu, c.ldb0 = h;
   c.out_split_row = 3 * h;
-  c.b_keep = true;
   (void)f;
   return c;
 }
