@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 // TMEM receives its 128 rows of the accumulator.  Per SM and 64-wide k-block
 // the stage is 32 KB instead of 48 KB, so the shared-memory traffic of TMA
 // writes plus operand reads drops by a third.
-//   warp 0      both ranks: TMA producer into their own ring of 5 or 6
+//   warp 0      both ranks: TMA producer into their own ring of 5
 //               stages (pair_stages).  The
 //               copies of both ranks complete on rank 0's `full` barrier of
 //               the stage (cta_group::2 TMA), which rank 0 arms with the
@@ -595,12 +595,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 // (256-row partial tiles, 8 arrival counters per tile).
 constexpr int kPairBN = 256;
 // Stages of the ring.  Fewer stages leave more of the SM's unified L1 /
-// shared memory to L1.  Measured at the 13B-class shapes: the
-// [out | down] and input-gradient GEMMs are 2.5-4.4% faster with 5 stages
-// than with 6, the [QKV | up] GEMM 1.7% slower; 7 stages (231 KB) were
-// 10-15% slower.
+// shared memory to L1.  With both operands loaded evict_last, 5 stages for
+// every GEMM against 6 for [QKV | up] (5 for the others): 175B-class layer
+// 4.41-4.47 vs 4.45-4.50 ms, 13B-class, e4m3 and training within noise; 6
+// for all and 7 for [QKV | up] were slower everywhere (175B-class 4.54-4.57
+// ms, training 14.3-14.7 vs 14.2-14.4 ms).  (Under the earlier evict_first
+// weights, 6 had been 1.7% better for [QKV | up] at 13B.)
 template <int EPI>
-__host__ __device__ constexpr int pair_stages() { return EPI == kEpiQkvGelu ? 6 : 5; }
+__host__ __device__ constexpr int pair_stages() { return 5; }
 template <bool STAGE = false, int NSTAGES = 6>
 struct PairCfg {
   static constexpr int kABytes = BM * 128;
