@@ -423,10 +423,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
-      // L2 priorities (measured on the forward GEMMs): the operand that is
-      // streamed once goes first, the one re-read by later tiles stays.
-      // Giving the forward weights normal priority slowed the 175B layer by
-      // 11%, and an L2 prefetch of the tiles 8 k-blocks ahead by 48%.
+      // L2 priority of each operand's loads as the launcher chose it (the
+      // layer's GEMMs keep both, evict_last).  Measured on this kernel with
+      // the weights at normal priority instead of evict_first, the 175B
+      // layer ran 11% slower; an L2 prefetch of the tiles 8 k-blocks ahead,
+      // 48% slower.
       const uint64_t pol = p.a_keep ? l2_policy_evict_last() : l2_policy_evict_first();
       const uint64_t pol_b = p.b_keep ? l2_policy_evict_last() : l2_policy_evict_first();
       int stage = 0;
