@@ -20,12 +20,14 @@ namespace {
 
 constexpr float kE4m3Max = 448.f;
 constexpr int kQThreads = 256;
+
 constexpr int kLnMaxVec = 16;  // 16-byte vectors of bf16 per thread -> H <= 32768
 
 __device__ __forceinline__ uint16_t e4m3x2(float a, float b) {
   return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
+template <int THREADS = kQThreads>
 __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -37,7 +39,7 @@ __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) 
   if ((threadIdx.x & 31) == 0) red[warp] = v;
   __syncthreads();
   float t = 0.f;  // both reductions here are of non-negative values or plain sums
-  for (int w = 0; w < kQThreads / 32; ++w) t = is_max ? fmaxf(t, red[w]) : t + red[w];
+  for (int w = 0; w < THREADS / 32; ++w) t = is_max ? fmaxf(t, red[w]) : t + red[w];
   return t;
 }
 
@@ -131,29 +133,35 @@ __global__ void __launch_bounds__(kQThreads) layernorm_fp8_kernel(
 // Row r of the output is [src0[r, 0:n0] | src1[r, 0:n1]] quantized with one
 // scale; written to out[(row0 + r) * (n0 + n1) ...] and scale[row0 + r].
 // Two passes over the row: the amax, then (re-reading the row, mostly from
-// L2) the quantized store.  Nothing is staged in shared memory, so eight
-// CTAs fit on an SM and the loads of one row overlap those of others.  (A
+// L2) the quantized store.  Nothing is staged in shared memory, so 2048
+// threads per SM (eight CTAs of 256 or two of 1024) keep loads in flight.
+// The rows in flight, one per CTA, must stay in L2 for the second pass, so
+// rows over 64 KB take 1024-thread CTAs: with 256-thread ones the 123 KB
+// rows of the 175B-shaped [ctx | G] (2048 x 61440) put ~150 MB in flight,
+// more than L2 (quantize 94 -> 77 us; the 530B shape 153 -> 130 us), while
+// the 51 KB rows of the 13B shape run faster on 256 (34 against 45 us).  (A
 // version that staged the row in shared memory ran one CTA per SM and took
-// 122 us for the 175B-shaped [ctx | G], 2048 x 61440.)
+// 122 us for the 175B shape.)
 __device__ __forceinline__ uint4 row_vec(const uint4* a, const uint4* b, int v0, int i) {
   return i < v0 ? __ldg(a + i) : __ldg(b + (i - v0));
 }
 
-__global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, 2048 / THREADS) quantize_rows_kernel(
     const __nv_bfloat16* __restrict__ src0, int64_t ld0, int n0,
     const __nv_bfloat16* __restrict__ src1, int64_t ld1, int n1, int64_t row0,
     uint8_t* __restrict__ out, float* __restrict__ scale) {
-  __shared__ float red[kQThreads / 32];
+  __shared__ float red[THREADS / 32];
   const int64_t r = blockIdx.x;
   const int v0 = n0 / 8, nv = (n0 + n1) / 8;
   const uint4* a = reinterpret_cast<const uint4*>(src0 + r * ld0);
   const uint4* b = src1 ? reinterpret_cast<const uint4*>(src1 + r * ld1) : a;
   float amax = 0.f;
   int i = threadIdx.x;
-  for (; i + 3 * kQThreads < nv; i += 4 * kQThreads) {  // four 16-byte loads in flight
+  for (; i + 3 * THREADS < nv; i += 4 * THREADS) {  // four 16-byte loads in flight
     uint4 c[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) c[u] = row_vec(a, b, v0, i + u * kQThreads);
+    for (int u = 0; u < 4; ++u) c[u] = row_vec(a, b, v0, i + u * THREADS);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const uint32_t w[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
@@ -162,18 +170,18 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
         amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
     }
   }
-  for (; i < nv; i += kQThreads) {
+  for (; i < nv; i += THREADS) {
     const uint4 c = row_vec(a, b, v0, i);
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
   }
-  amax = block_reduce(amax, red, true);
+  amax = block_reduce<THREADS>(amax, red, true);
   const float s = amax > 0.f ? amax / kE4m3Max : 1.f;
   const float inv = 1.f / s;
   uint2* dst = reinterpret_cast<uint2*>(out + (row0 + r) * static_cast<int64_t>(n0 + n1));
-  for (int j = threadIdx.x; j < nv; j += kQThreads) {
+  for (int j = threadIdx.x; j < nv; j += THREADS) {
     const uint4 c = row_vec(a, b, v0, j);
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
     float f[8];
@@ -221,8 +229,12 @@ cudaError_t launch_quantize_rows(const __nv_bfloat16* src0, int64_t ld0, int n0,
                                  int64_t row0, uint8_t* out, float* scale, cudaStream_t stream) {
   if (n0 % 8 || n1 % 8 || n0 + n1 <= 0 || rows > 0x7fffffff) return cudaErrorInvalidValue;
   if (rows <= 0) return cudaSuccess;
-  quantize_rows_kernel<<<static_cast<unsigned>(rows), kQThreads, 0, stream>>>(
-      src0, ld0, n0, src1, ld1, n1, row0, out, scale);
+  if (2 * static_cast<int64_t>(n0 + n1) > (int64_t{64} << 10))
+    quantize_rows_kernel<1024><<<static_cast<unsigned>(rows), 1024, 0, stream>>>(
+        src0, ld0, n0, src1, ld1, n1, row0, out, scale);
+  else
+    quantize_rows_kernel<256><<<static_cast<unsigned>(rows), 256, 0, stream>>>(
+        src0, ld0, n0, src1, ld1, n1, row0, out, scale);
   return cudaGetLastError();
 }
 
