@@ -387,10 +387,14 @@ def test_ptb_forward_fp8_small(ptb_lib, cfg):
     _fp8_check(ptb_lib, cfg, host, d, list(range(cfg.seq)), cfg.name)
 
 
-def test_fp8_weight_codes_bit_exact(ptb_lib):
+@pytest.mark.parametrize("cfg", [workloads.small_ptb(1, 64, 384, 4, 1536, 16, seed=27),
+                                 # [W_o | W_down] rows of 33536 elements (67 KB): the
+                                 # quantizer's long-row CTA shape
+                                 workloads.small_ptb(1, 64, 256, 2, 33280, 16, seed=28)],
+                         ids=lambda c: c.name)
+def test_fp8_weight_codes_bit_exact(ptb_lib, cfg):
     """The e4m3 weight codes and per-row scales are integer decisions taken in
     fp32; they must match an fp32 CPU computation bit for bit."""
-    cfg = workloads.small_ptb(1, 64, 384, 4, 1536, 16, seed=27)
     d = _cuda(workloads.ptb_inputs(cfg))
     w1, s1, w2, s2 = ptb_lib.prepare_fp8_weights(d["w_qkv"], d["w_o"], d["w_up"], d["w_down"])
     torch.cuda.synchronize()
@@ -403,6 +407,12 @@ def test_fp8_weight_codes_bit_exact(ptb_lib):
     wz[5].zero_()
     _, s1z, _, _ = ptb_lib.prepare_fp8_weights(d["w_qkv"], d["w_o"], wz, d["w_down"])
     assert float(s1z[3 * cfg.hidden + 5]) == 1.0
+    # The same for a row of [W_o | W_down].
+    woz, wdz = d["w_o"].clone(), d["w_down"].clone()
+    woz[7].zero_()
+    wdz[7].zero_()
+    _, _, w2z, s2z = ptb_lib.prepare_fp8_weights(d["w_qkv"], woz, d["w_up"], wdz)
+    assert float(s2z[7]) == 1.0 and int(w2z[7].abs().sum()) == 0
 
 
 @pytest.mark.parametrize("name", ["13b", "175b", "530b"])
