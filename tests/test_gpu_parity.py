@@ -530,3 +530,28 @@ def test_forward_host_buffers_two_streams(ptb_lib):
                                  stream=streams[i])
     torch.cuda.synchronize()
     assert torch.equal(ys[0], want) and torch.equal(ys[1], want2)
+
+
+def test_forward_host_buffers_two_streams_serialised(ptb_lib):
+    """The same for a layer whose first GEMM exceeds 2^39 multiply-adds,
+    where each call's layer waits for the previous call's layer on the other
+    stream (the path of the large layers): still the bits of ptb_forward."""
+    cfg = workloads.small_ptb(1, 2048, 6144, 48, 32768, 512, seed=45)
+    assert cfg.batch * cfg.seq * cfg.hidden * (3 * cfg.hidden + cfg.ffn) > 2 ** 39
+    d = {k: v.cuda() for k, v in workloads.ptb_inputs(cfg).items()}
+    w = (d["ln_gamma"], d["ln_beta"], d["w_qkv"], d["w_o"], d["w_up"], d["w_down"])
+    x2 = workloads.normal_bf16(tuple(d["x"].shape), seed=46)
+    want = ptb_lib.ptb_forward(d["x"], *w, cfg.heads, cfg.window).cpu()
+    want2 = ptb_lib.ptb_forward(x2.cuda(), *w, cfg.heads, cfg.window).cpu()
+    xs = [d["x"].cpu().pin_memory(), x2.pin_memory()]
+    ys = [torch.full_like(xs[0], float("nan")).pin_memory() for _ in range(2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    nbytes = ptb_lib.host_workspace_size(cfg.batch, cfg.seq, cfg.hidden, cfg.ffn)
+    wss = [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    for rep in range(2):  # the second round waits on the first round's layers
+        for i in range(2):
+            ptb_lib.ptb_forward_host(xs[i], *w, cfg.heads, cfg.window, ys[i], wss[i],
+                                     stream=streams[i])
+    torch.cuda.synchronize()
+    assert torch.equal(ys[0], want) and torch.equal(ys[1], want2)
+    assert ptb_lib.last_device_error() == 0
